@@ -1,0 +1,210 @@
+"""Python binding of libfa (exact attention for GB300 / sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of libfa.so.  The C functions keep their names (`fa_fwd`, `fa_bwd`,
+...); each takes device pointers (ints or torch CUDA tensors) and raises
+`FaError` on a non-OK status.  `forward` / `backward` are conveniences that
+allocate the outputs with torch and call the same C functions.
+
+Importing this package fails loudly if libfa.so has not been built
+(`python -c "import __graft_entry__ as g; g.build()"`): there is no fallback.
+"""
+import ctypes
+import os
+
+__all__ = [
+    "FaError", "FaMask", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
+    "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_fwd_fp32", "fa_bwd_fp32",
+    "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
+    "make_mask", "forward", "backward", "LIB_PATH",
+    "FA_MASK_NONE", "FA_MASK_KEY_PADDING", "FA_MASK_BLOCK_SPARSE", "STATUS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+FA_MASK_NONE, FA_MASK_KEY_PADDING, FA_MASK_BLOCK_SPARSE = 0, 1, 2
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_ALIGNMENT",
+          4: "FA_ERR_WORKSPACE", 5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT"}
+
+
+class FaError(RuntimeError):
+    def __init__(self, code, where):
+        self.code = code
+        super().__init__("%s returned %s" % (where, STATUS.get(code, code)))
+
+
+class FaMask(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("kv_len", ctypes.c_void_p),
+                ("block_mask", ctypes.c_void_p), ("block_size", ctypes.c_int)]
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libfa.so is not built (expected at %s); run "
+                      "__graft_entry__.build() first" % LIB_PATH)
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+_mp = ctypes.POINTER(FaMask)
+
+_SIGS = {
+    "fa_fwd": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_fwd_fp32": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_bwd_workspace_size": [_i, _i, _i, _i],
+    "fa_bwd": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_bwd_fp32": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_bwd_preprocess": [_p, _p, _p, _p, _i, _i, _i, _i, _p],
+    "fa_bwd_dkdv": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_bwd_dq_convert": [_p, _p, _i, _i, _i, _i, _p],
+    "fa_status_string": [_i],
+    "fa_get_device_status": [_p, ctypes.POINTER(ctypes.c_int)],
+    "fa_debug_umma_gemm": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p],
+    "fa_debug_wait_timeout": [ctypes.c_uint, _p],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = ctypes.c_int
+lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
+lib.fa_status_string.restype = ctypes.c_char_p
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+def _check(code, where):
+    if code != 0:
+        raise FaError(code, where)
+
+
+def make_mask(kv_len=None, block_mask=None, block_size=128):
+    """A pointer to an fa_mask for key padding (kv_len) or a block-sparse tile
+    mask (device tensors), or None for no mask."""
+    if kv_len is not None and block_mask is not None:
+        raise ValueError("one mask kind at a time")
+    if kv_len is not None:
+        return ctypes.pointer(FaMask(FA_MASK_KEY_PADDING, _ptr(kv_len), None, block_size))
+    if block_mask is not None:
+        return ctypes.pointer(FaMask(FA_MASK_BLOCK_SPARSE, None, _ptr(block_mask), block_size))
+    return None
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, stream=None):
+    _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                      int(causal), mask, _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_fp32(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, stream=None):
+    _check(lib.fa_fwd_fp32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                           int(causal), mask, _stream(stream)), "fa_fwd_fp32")
+
+
+def fa_bwd_workspace_size(B, H, N, d):
+    return lib.fa_bwd_workspace_size(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
+           causal, mask=None, stream=None):
+    _check(lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                      _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, B, H, N, d, scale,
+                      int(causal), mask, _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_fp32(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
+                causal, mask=None, stream=None):
+    _check(lib.fa_bwd_fp32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, B, H, N, d,
+                           scale, int(causal), mask, _stream(stream)), "fa_bwd_fp32")
+
+
+def fa_bwd_preprocess(o, dO, D, dq_acc, B, H, N, d, stream=None):
+    _check(lib.fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), _ptr(dq_acc), B, H, N, d,
+                                 _stream(stream)), "fa_bwd_preprocess")
+
+
+def fa_bwd_dkdv(q, k, v, dO, lse, D, dq_acc, dk, dv, B, H, N, d, scale, causal, mask=None,
+                stream=None):
+    _check(lib.fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
+                           _ptr(dq_acc), _ptr(dk), _ptr(dv), B, H, N, d, scale, int(causal),
+                           mask, _stream(stream)), "fa_bwd_dkdv")
+
+
+def fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, stream=None):
+    _check(lib.fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, _stream(stream)),
+           "fa_bwd_dq_convert")
+
+
+def fa_status_string(code):
+    return lib.fa_status_string(code).decode()
+
+
+def fa_get_device_status(stream=None):
+    """(status code, site) after synchronizing `stream`."""
+    site = ctypes.c_int(0)
+    code = lib.fa_get_device_status(_stream(stream), ctypes.byref(site))
+    return code, site.value
+
+
+def fa_debug_umma_gemm(a, b, d, M, N, K, a_mn_major=0, b_mn_major=0, a_in_tmem=0, use_tma=0,
+                       stream=None):
+    _check(lib.fa_debug_umma_gemm(_ptr(a), _ptr(b), _ptr(d), M, N, K, a_mn_major, b_mn_major,
+                                  a_in_tmem, use_tma, _stream(stream)), "fa_debug_umma_gemm")
+
+
+def fa_debug_wait_timeout(limit_us, stream=None):
+    _check(lib.fa_debug_wait_timeout(limit_us, _stream(stream)), "fa_debug_wait_timeout")
+
+
+# ---------------------------------------------------------------------------
+# conveniences: allocate outputs with torch, call the C functions
+# ---------------------------------------------------------------------------
+
+def _shape(q):
+    if q.dim() != 4:
+        raise ValueError("expected [B, H, N, d]")
+    return tuple(int(x) for x in q.shape)
+
+
+def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None):
+    """(O, lse) for contiguous CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32)."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    mask = make_mask(kv_len, block_mask)
+    fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_fp32
+    fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_mask=None,
+             stream=None, workspace=None):
+    """(dQ, dK, dV) for the forward above and output gradient do."""
+    import torch
+    B, H, N, d = _shape(q)
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_workspace_size(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    mask = make_mask(kv_len, block_mask)
+    fn = fa_bwd if q.dtype == torch.bfloat16 else fa_bwd_fp32
+    fn(q, k, v, o, do, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, mask,
+       stream)
+    return dq, dk, dv

@@ -1,0 +1,324 @@
+// The exported C ABI of libfa: argument validation (on the host, before any
+// CUDA runtime call), TMA descriptor encoding, the device status block, and
+// dispatch to the kernel launchers of the other translation units.
+#include <math.h>
+
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+// 4-int status block per device (a __device__ variable: no allocation).
+__device__ int g_status[4];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool scale_ok(float s) { return s > 0.f && s != INFINITY; }  // false for NaN too
+
+fa_status check_sizes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H > 65535) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H * N * d > (1ll << 40)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_mask(const fa_mask* m, int* kind, const int32_t** kv, const uint8_t** bm) {
+  *kind = FA_MASK_NONE;
+  *kv = nullptr;
+  *bm = nullptr;
+  if (!m) return FA_OK;
+  switch (m->kind) {
+    case FA_MASK_NONE:
+      return FA_OK;
+    case FA_MASK_KEY_PADDING:
+      if (!m->kv_len || !aligned4(m->kv_len)) return FA_ERR_INVALID_ARG;
+      *kind = FA_MASK_KEY_PADDING;
+      *kv = m->kv_len;
+      return FA_OK;
+    case FA_MASK_BLOCK_SPARSE:
+      if (!m->block_mask) return FA_ERR_INVALID_ARG;
+      if (m->block_size != 128) return FA_ERR_UNSUPPORTED;
+      *kind = FA_MASK_BLOCK_SPARSE;
+      *bm = m->block_mask;
+      return FA_OK;
+    default:
+      return FA_ERR_INVALID_ARG;
+  }
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int* device_status() {
+  static int* ptrs[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+// Looked up only once every argument has been validated, so that argument
+// errors are reported without touching the CUDA runtime.
+template <typename Args>
+static bool attach_status(Args* a) {
+  a->status = device_status();
+  return a->status != nullptr;
+}
+
+static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* v, void* o,
+                          float* lse, int B, int H, int N, int d, float scale, int causal,
+                          const fa_mask* mask) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
+    return FA_ERR_ALIGNMENT;
+  st = check_mask(mask, &a->mask_kind, &a->kv_len, &a->block_mask);
+  if (st != FA_OK) return st;
+  a->q = q; a->k = k; a->v = v; a->o = o; a->lse = lse;
+  a->B = B; a->H = H; a->N = N; a->d = d;
+  a->scale = scale;
+  a->causal = causal;
+  return FA_OK;
+}
+
+static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float scale, int causal,
+                                 const fa_mask* mask) {
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
+  st = check_mask(mask, &a->mask_kind, &a->kv_len, &a->block_mask);
+  if (st != FA_OK) return st;
+  a->B = B; a->H = H; a->N = N; a->d = d;
+  a->scale = scale;
+  a->causal = causal;
+  return FA_OK;
+}
+
+static fa_status split_workspace(BwdArgs* a, void* ws, size_t ws_bytes) {
+  if (!ws) return FA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return FA_ERR_ALIGNMENT;
+  if (ws_bytes < round256((size_t)a->B * a->H * a->N * sizeof(float)) +
+                     round256((size_t)a->B * a->H * a->N * a->d * sizeof(float)))
+    return FA_ERR_WORKSPACE;
+  const size_t rows = (size_t)a->B * a->H * a->N;
+  a->D = static_cast<float*>(ws);
+  a->dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round256(rows * sizeof(float)));
+  return FA_OK;
+}
+
+static fa_status launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported size or option";
+    case FA_ERR_ALIGNMENT: return "FA_ERR_ALIGNMENT: tensor pointer not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace missing or too small";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait gave up";
+  }
+  return "unknown fa_status";
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA_OK) return 0;
+  const size_t rows = (size_t)B * H * N;
+  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, const fa_mask* mask, void* stream) {
+  FwdArgs a{};
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                      void* stream) {
+  FwdArgs a{};
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_fwd_fp32(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                 const fa_mask* mask, void* stream) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  st = split_workspace(&a, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_bwd_preprocess(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  if (launch_bwd_dkdv_bf16(a, s) != cudaSuccess) return FA_ERR_CUDA;
+  return launched(launch_bwd_dq_convert(a, s));
+}
+
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H,
+                            int N, int d, void* stream) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr);
+  if (st != FA_OK) return st;
+  if (!o || !dO || !D || !dq_acc) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned4(D) || !aligned16(dq_acc))
+    return FA_ERR_ALIGNMENT;
+  a.o = o; a.dO = dO; a.D = D; a.dq_acc = dq_acc;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_bwd_preprocess(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                      const float* lse, const float* D, float* dq_acc, void* dk, void* dv, int B,
+                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                      void* stream) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !dO || !lse || !D || !dq_acc || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
+      !aligned4(D) || !aligned16(dq_acc) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  a.q = q; a.k = k; a.v = v; a.dO = dO; a.lse = lse;
+  a.D = const_cast<float*>(D); a.dq_acc = dq_acc; a.dk = dk; a.dv = dv;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
+                            void* stream) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr);
+  if (st != FA_OK) return st;
+  if (!dq_acc || !dq) return FA_ERR_INVALID_ARG;
+  if (!aligned16(dq_acc) || !aligned16(dq)) return FA_ERR_ALIGNMENT;
+  a.dq_acc = const_cast<float*>(dq_acc); a.dq = dq;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_bwd_dq_convert(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const float* o,
+                      const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                      float scale, int causal, const fa_mask* mask, void* stream) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  st = split_workspace(&a, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
+  a.dq = dq; a.dk = dk; a.dv = dv;
+  if (!attach_status(&a)) return FA_ERR_CUDA;
+  return launched(launch_bwd_fp32(a, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_get_device_status(void* stream, int* site) {
+  if (site) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int* st = device_status();
+  if (!st) return FA_ERR_CUDA;
+  int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, st, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (h[0] != 0) {
+    if (site) *site = h[1];
+    const int z[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(st, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+    return h[0] == kStatusTimeoutCode ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
+  }
+  return FA_OK;
+}
+
+fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int N, int K,
+                             int a_mn_major, int b_mn_major, int a_in_tmem, int use_tma,
+                             void* stream) {
+  if (!a || !b || !d) return FA_ERR_INVALID_ARG;
+  if (M != 128 || (N != 64 && N != 128 && N != 256) || (K != 64 && K != 128))
+    return FA_ERR_UNSUPPORTED;
+  if (a_in_tmem < 0 || a_in_tmem > 3 || (a_in_tmem && a_mn_major)) return FA_ERR_INVALID_ARG;
+  if (use_tma && (a_mn_major || b_mn_major)) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FA_ERR_ALIGNMENT;
+  int* st = device_status();
+  if (!st) return FA_ERR_CUDA;
+  return launched(launch_umma_probe(a, b, d, M, N, K, a_mn_major, b_mn_major, a_in_tmem, use_tma,
+                                    st, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID_ARG;
+  int* st = device_status();
+  if (!st) return FA_ERR_CUDA;
+  return launched(launch_wait_probe(1000ull * limit_us, st, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+/*
+ * fa.h -- C ABI of libfa, exact attention for NVIDIA GB300 (sm_103a).
+ *
+ * Computes, for every batch element b and head h (the plain definition of
+ * attention: "FlashAttention: Fast and Memory-Efficient Exact Attention with
+ * IO-Awareness", summary page, "Problem and motivation"; scale on the scores
+ * as in the GitHub issue "Fewer matrix multiplications, same results"):
+ *
+ *     S   = scale * Q K^T      (entries of invisible keys are -inf)
+ *     P   = softmax(S)         (row-wise, with the row maximum subtracted)
+ *     O   = P V
+ *     lse = ln sum_j exp(S_ij)  (natural log; the only statistic kept)
+ *
+ * tile by tile with the online-softmax recurrence (blog review "From Online
+ * Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)"; summary
+ * page, "Method": running max m, running denominator l, rescaled output), so
+ * the N x N score matrix never reaches device memory, and the backward pass
+ * recomputes P on chip from Q, K and lse (summary page, "Key ideas:
+ * recomputation in the backward pass").
+ *
+ * Conventions shared by every call:
+ *   - Tensors are dense row-major [B, H, N, d] (d contiguous) in DEVICE
+ *     memory, 16-byte aligned; lse and D are fp32 [B, H, N].  The caller owns
+ *     every buffer; the library allocates nothing.
+ *   - bf16 calls take bf16 (uint16 storage) Q, K, V, O, dO, dQ, dK, dV and
+ *     accumulate in fp32.  *_fp32 calls take fp32 everywhere.
+ *   - d must be 64 or 128; N >= 1 (any N: ragged tails are masked); B >= 1,
+ *     H >= 1, B*H <= 65535; scale must be positive and finite.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous with respect to the host, like cuBLAS: a returned
+ *     FA_OK means the work was enqueued.
+ *   - Argument errors are detected on the host before anything is launched
+ *     (and before any CUDA runtime call), and reported through the return
+ *     value only.
+ *   - Masking: `causal` keeps keys j <= i (queries and keys share indices).
+ *     `mask` may add key padding (keys j >= kv_len[b] are invisible) or a
+ *     block-sparse tile mask (tile (i/128, j/128) visible iff
+ *     block_mask[(i/128)*T + j/128] != 0, T = ceil(N/128); summary page,
+ *     "Extension: block-sparse FlashAttention").  causal combines with either
+ *     (intersection).  A query row with no visible key gets O = 0,
+ *     lse = -inf and contributes no gradient.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad mask kind  */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (d not 64/128, ...)   */
+  FA_ERR_ALIGNMENT = 3,    /* a tensor pointer is not 16-byte aligned         */
+  FA_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required      */
+  FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed               */
+  FA_ERR_TIMEOUT = 6       /* a kernel gave up waiting (see fa_get_device_status) */
+} fa_status;
+
+typedef enum {
+  FA_MASK_NONE = 0,
+  FA_MASK_KEY_PADDING = 1,
+  FA_MASK_BLOCK_SPARSE = 2
+} fa_mask_kind;
+
+typedef struct {
+  int kind;                  /* an fa_mask_kind                                     */
+  const int32_t* kv_len;     /* KEY_PADDING: device int32 [B]; values are clamped   */
+                             /* to 0..N (0 = every key of the batch is padding)     */
+  const uint8_t* block_mask; /* BLOCK_SPARSE: device uint8 [T*T], T = ceil(N/128)   */
+  int block_size;            /* BLOCK_SPARSE: tile edge of block_mask, must be 128  */
+} fa_mask;
+
+/* Forward pass, bf16 in/out.
+ *   q, k, v : [B,H,N,d] bf16 inputs.   o : [B,H,N,d] bf16 output.
+ *   lse     : [B,H,N] fp32 output, natural-log log-sum-exp of each score row
+ *             (-inf for a row with no visible key).
+ *   scale   : multiplies Q K^T (1/sqrt(d) for standard attention).
+ *   causal  : 0 or 1.   mask : NULL for none.
+ * Summary page "Method" (block statistics m, l and the rescaled output) and
+ * blog review "Algorithm FlashAttention (Tiling)". */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, const fa_mask* mask, void* stream);
+
+/* Bytes of device workspace fa_bwd / fa_bwd_fp32 need: D (fp32 [B,H,N]) plus
+ * an fp32 dQ accumulator [B,H,N,d], each padded to 256 bytes.  0 on bad sizes. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/* Backward pass, bf16.  Given the forward's inputs, its outputs o and lse,
+ * and the output gradient dO, writes dq, dk, dv ([B,H,N,d] bf16) for the loss
+ * whose gradient with respect to O is dO.  P is recomputed from q, k, lse
+ * (summary page, "Key ideas: recomputation in the backward pass"); the
+ * gradient formulas (dV = P^T dO, dP = dO V^T, D = rowsum(dO o O),
+ * dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q) are the textbook
+ * derivative, which the pages do not write out.
+ *   workspace : device, >= fa_bwd_workspace_size(B,H,N,d) bytes, 16-byte
+ *               aligned; contents on entry are ignored.
+ * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert on `stream`. */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                 size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                 const fa_mask* mask, void* stream);
+
+/* The three steps of fa_bwd, exposed for timing each kernel on its own.
+ * fa_bwd_preprocess: D[b,h,i] = sum_c dO[b,h,i,c] * O[b,h,i,c] (fp32), and
+ *   sets dq_acc (fp32 [B,H,N,d]) to zero.
+ * fa_bwd_dkdv: recomputes P and dS tile by tile, writes dk, dv (bf16) and
+ *   adds scale * dS K into dq_acc.  D and dq_acc as left by the preprocess.
+ * fa_bwd_dq_convert: dq (bf16) = dq_acc (fp32), round to nearest even. */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H,
+                            int N, int d, void* stream);
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                      const float* lse, const float* D, float* dq_acc, void* dk, void* dv, int B,
+                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                      void* stream);
+fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
+                            void* stream);
+
+/* fp32 twins of fa_fwd / fa_bwd: identical argument meaning with fp32
+ * tensors everywhere (CUDA cores, no tensor cores; for small fp32 workloads). */
+fa_status fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                      void* stream);
+fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const float* o,
+                      const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                      void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                      float scale, int causal, const fa_mask* mask, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/* Synchronizes `stream`, then reports and clears the device-side status that
+ * the kernels raise when a wait inside them gives up (FA_ERR_TIMEOUT), or
+ * FA_ERR_CUDA if the stream reports an error.  FA_OK otherwise.  If site is
+ * not NULL it receives the id of the wait that gave up. */
+fa_status fa_get_device_status(void* stream, int* site);
+
+/* Diagnostic: one CTA computes D[M x N] (fp32, row-major) = A B^T on the
+ * tensor cores with exactly the operand staging the attention kernels use,
+ * so a GPU can be checked for the layouts they rely on.
+ *   a : device bf16 [M x K] row-major, b : device bf16 [N x K] row-major,
+ *   M = 128, N in {64, 128, 256}, K in {64, 128}.
+ *   a_mn_major / b_mn_major : stage the operand M/N-contiguous instead of
+ *   K-contiguous.  a_in_tmem : 0 = A from shared memory; 1 = A from tensor
+ *   memory, two bf16 per 32-bit column, even k in the low half; 2 = the same
+ *   with even k in the high half; 3 = one bf16 per column (1..3 need
+ *   a_mn_major = 0).  use_tma : load K-major operands with TMA instead of
+ *   plain loads. */
+fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int N, int K,
+                             int a_mn_major, int b_mn_major, int a_in_tmem, int use_tma,
+                             void* stream);
+
+/* Diagnostic: launches one CTA that waits on an mbarrier no one arrives on,
+ * with the given limit (1..1000000 microseconds), exactly as the attention
+ * kernels bound their waits.  The kernel returns normally; a following
+ * fa_get_device_status reports FA_ERR_TIMEOUT.  Lets the failure path be
+ * checked without hanging or faulting a GPU. */
+fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -18,4 +18,5 @@ from .attention import (  # noqa: F401
     softmax_three_pass,
     softmax_online_two_pass,
     attention_row_one_pass_tiled,
+    row_block_forward_backward,
 )

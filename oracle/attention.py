@@ -56,7 +56,7 @@ __all__ = [
     "visible", "scores", "probabilities", "forward", "backward",
     "forward_rows", "backward_query_rows", "backward_key_rows", "row_stats",
     "softmax_three_pass", "softmax_online_two_pass",
-    "attention_row_one_pass_tiled",
+    "attention_row_one_pass_tiled", "row_block_forward_backward",
 ]
 
 
@@ -258,6 +258,30 @@ def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=No
             dv[b, h] = p.T @ dof
             dk[b, h] = scale * (ds.T @ qf)
     return dk, dv
+
+
+def row_block_forward_backward(q, k, v, do, scale, b, h, rows, causal=False, kv_len=None,
+                               block_mask=None, block=128):
+    """Forward and backward of one block of query rows of slice (b, h), the
+    definition restricted to those rows: O, lse and dQ of the rows, and the
+    rows' contributions P^T dO and scale dS^T Q to dV and dK.  Summing the
+    contributions of every row block gives the full dK, dV."""
+    r = np.asarray(rows, np.int64)
+    N = k.shape[2]
+    vis = visible(r, N, causal, _kv_len_of(kv_len, b), block_mask, block)
+    qf = np.asarray(q[b, h][r], np.float64)
+    kf = np.asarray(k[b, h], np.float64)
+    vf = np.asarray(v[b, h], np.float64)
+    dof = np.asarray(do[b, h][r], np.float64)
+    p, lse = probabilities(scores(qf, kf, scale, vis))
+    o = p @ vf
+    dp = dof @ vf.T
+    d_row = np.sum(p * dp, axis=1)
+    ds = p * (dp - d_row[:, None])
+    dq = scale * (ds @ kf)
+    dk_part = scale * (ds.T @ qf)
+    dv_part = p.T @ dof
+    return o, lse, dq, dk_part, dv_part
 
 
 # --------------------------------------------------------------------------

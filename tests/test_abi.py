@@ -1,0 +1,131 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/fa.h declares, and rejects bad arguments on the host before touching
+the CUDA runtime."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    # These calls pass fake (never dereferenced) pointers that validation must
+    # reject; keep them off machines with a GPU so that a validation bug can
+    # never turn into a launch with bad pointers.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only validation tests run on machines without a GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_88_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+                     "fa_get_device_status", "fa_fwd_fp32", "fa_bwd_fp32"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(fa):
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s+(\S+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(fa.lib, n)
+
+
+def test_status_strings(fa):
+    for code, name in fa.STATUS.items():
+        assert fa.fa_status_string(code).startswith(name)
+    assert "unknown" in fa.fa_status_string(99)
+
+
+def test_workspace_size(fa):
+    B, H, N, d = 2, 3, 1000, 128
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
+    assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def fwd(fa, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+             causal=0, mask=None)
+    a.update(kw)
+    return fa.lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                         a["d"], a["scale"], a["causal"], a["mask"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(lse=0), 1), (dict(B=0), 1), (dict(N=0), 1), (dict(N=-5), 1),
+    (dict(d=96), 2), (dict(d=256), 2), (dict(B=300, H=300), 2),
+    (dict(causal=2), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(q=FAKE + 8), 3), (dict(o=FAKE + 2), 3), (dict(lse=FAKE + 2), 3),
+])
+def test_fwd_rejects_bad_arguments(fa, kw, code):
+    assert fwd(fa, **kw) == code
+    assert fa.lib.fa_fwd_fp32(kw.get("q", FAKE), FAKE, FAKE, kw.get("o", FAKE),
+                              kw.get("lse", FAKE), kw.get("B", 1), kw.get("H", 1),
+                              kw.get("N", 128), kw.get("d", 64), kw.get("scale", 0.125),
+                              kw.get("causal", 0), None, None) == code
+
+
+def test_fwd_rejects_bad_masks(fa):
+    m = ctypes.pointer(fa.FaMask(7, None, None, 128))
+    assert fwd(fa, mask=m) == 1
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_KEY_PADDING, None, None, 0))
+    assert fwd(fa, mask=m) == 1   # NULL kv_len
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_KEY_PADDING, FAKE + 2, None, 0))
+    assert fwd(fa, mask=m) == 1   # misaligned kv_len
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, FAKE, None, 128))
+    assert fwd(fa, mask=m) == 1   # NULL block mask
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 64))
+    assert fwd(fa, mask=m) == 2   # only 128-wide tiles
+
+
+def bwd(fa, **kw):
+    B, H, N, d = kw.get("B", 1), kw.get("H", 1), kw.get("N", 128), kw.get("d", 64)
+    ws = kw.get("ws_bytes", fa.fa_bwd_workspace_size(1, 1, 128, 64))
+    return fa.lib.fa_bwd(kw.get("q", FAKE), FAKE, FAKE, FAKE, kw.get("dO", FAKE), FAKE,
+                         kw.get("dq", FAKE), FAKE, FAKE, kw.get("ws", FAKE), ws, B, H, N, d,
+                         kw.get("scale", 0.125), 0, None, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(dO=0), 1), (dict(dq=FAKE + 4), 3), (dict(d=32), 2),
+    (dict(ws=0), 4), (dict(ws_bytes=100), 4), (dict(ws=FAKE + 8), 3), (dict(scale=-0.1), 1),
+])
+def test_bwd_rejects_bad_arguments(fa, kw, code):
+    assert bwd(fa, **kw) == code
+
+
+def test_substeps_reject_bad_arguments(fa):
+    assert fa.lib.fa_bwd_preprocess(0, FAKE, FAKE, FAKE, 1, 1, 128, 64, None) == 1
+    assert fa.lib.fa_bwd_preprocess(FAKE, FAKE, FAKE, FAKE + 4, 1, 1, 128, 64, None) == 3
+    assert fa.lib.fa_bwd_dq_convert(FAKE, 0, 1, 1, 128, 64, None) == 1
+    assert fa.lib.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128,
+                              80, 0.1, 0, None, None) == 2
+    assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 64, 128, 64, 0, 0, 0, 0, None) == 2
+    assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 1, 0, 1, 0, None) == 1
+    assert fa.lib.fa_debug_wait_timeout(0, None) == 1
+    assert fa.lib.fa_debug_wait_timeout(2000000, None) == 1

@@ -432,3 +432,27 @@ def test_sampled_rows_equal_full(kind):
     dk_c, dv_c = A.backward_key_rows(q, k, v, do, s, cols, lse_all, dd_all, **ma)
     assert np.max(np.abs(dk_c - take(dk, cols))) <= 1e-12
     assert np.max(np.abs(dv_c - take(dv, cols))) <= 1e-12
+
+
+@pytest.mark.parametrize("kind", ["causal", "padding", "sparse"])
+def test_row_blocks_sum_to_full_backward(kind):
+    """Row-block pieces (used to time a bounded sample) reassemble the full result."""
+    B, H, N, d = 2, 1, 45, 8
+    q, k, v, do = (rand((B, H, N, d), 110 + i) for i in range(4))
+    ma = mask_args(kind, B, N, 115, block=16)
+    o, lse = A.forward(q, k, v, 0.3, **ma)
+    dq, dk, dv, _ = A.backward(q, k, v, do, 0.3, **ma)
+    for b in range(B):
+        dk_sum = np.zeros((N, d))
+        dv_sum = np.zeros((N, d))
+        for r0 in range(0, N, 10):
+            r = np.arange(r0, min(N, r0 + 10))
+            ob, lb, dqb, dkp, dvp = A.row_block_forward_backward(q, k, v, do, 0.3, b, 0, r, **ma)
+            assert np.max(np.abs(ob - o[b, 0, r])) <= 1e-13
+            fin = np.isfinite(lse[b, 0, r])
+            assert np.max(np.abs((lb - lse[b, 0, r])[fin])) <= 1e-13
+            assert np.max(np.abs(dqb - dq[b, 0, r])) <= 1e-12
+            dk_sum += dkp
+            dv_sum += dvp
+        assert np.max(np.abs(dk_sum - dk[b, 0])) <= 1e-12
+        assert np.max(np.abs(dv_sum - dv[b, 0])) <= 1e-12

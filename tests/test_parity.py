@@ -1,0 +1,158 @@
+"""GPU parity: libfa through its C ABI against the fp64 oracle on the same
+seeded inputs, element by element, within the stated tolerances
+(bf16: O max-abs 1e-2, lse max-abs 1e-3, dQ/dK/dV relative Frobenius 2e-2;
+fp32: ten times tighter)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, generate, random_case
+from _gpu_helpers import TOL, f64, max_abs, rel_fro, run, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def check_full(fa, case, B, H, N, d, causal, dtype, bwd=True):
+    scale = d ** -0.5
+    t = to_device(case, dtype)
+    o, lse, grads = run(fa, t, scale, causal, with_bwd=bwd)
+    kw = dict(causal=causal, kv_len=case.get("kv_len"), block_mask=case.get("block_mask"))
+    ro, rl = oracle.forward(case["q"], case["k"], case["v"], scale, **kw)
+    to, tl, tg = TOL[dtype]
+    e_o = max_abs(f64(o), ro)
+    e_l = max_abs(lse.cpu().numpy().astype(np.float64), rl, finite_only=True)
+    assert np.array_equal(np.isneginf(lse.cpu().numpy()), np.isneginf(rl)), "empty-row pattern"
+    assert e_o <= to, ("O", e_o)
+    assert e_l <= tl, ("lse", e_l)
+    if bwd:
+        rdq, rdk, rdv, _ = oracle.backward(case["q"], case["k"], case["v"], case["do"], scale, **kw)
+        for name, g, r in zip(("dQ", "dK", "dV"), grads, (rdq, rdk, rdv)):
+            e = rel_fro(f64(g), r)
+            assert e <= tg, (name, e)
+    return o, lse, grads
+
+
+SMALL = [
+    # B, H, N, d, causal, mask
+    (1, 2, 128, 64, False, "none"),
+    (1, 2, 128, 128, True, "none"),
+    (2, 2, 300, 64, True, "none"),        # ragged tail
+    (1, 1, 1, 64, False, "none"),         # a single token
+    (1, 2, 77, 128, False, "none"),       # shorter than one tile
+    (1, 1, 1000, 64, True, "none"),       # many tiles, ragged
+    (1, 2, 513, 128, False, "none"),
+    (2, 3, 384, 64, False, "padding"),
+    (2, 2, 512, 128, True, "padding"),
+    (1, 2, 640, 64, False, "sparse"),
+    (1, 2, 520, 128, True, "sparse"),
+]
+
+
+def small_case(B, H, N, d, mask, seed, dtype="bf16"):
+    rng = np.random.default_rng(seed + 99)
+    kv = bm = None
+    if mask == "padding":
+        kv = rng.integers(1, N + 1, B)
+        kv[0] = min(N, 100)
+    if mask == "sparse":
+        T = (N + 127) // 128
+        bm = (rng.random((T, T)) < 0.35).astype(np.uint8)
+        bm[np.arange(T), np.arange(T)] = 1
+    return random_case(B, H, N, d, seed, dtype=dtype, kv_len=kv, block_mask=bm)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,mask", SMALL)
+def test_small_bf16(fa, B, H, N, d, causal, mask):
+    case = small_case(B, H, N, d, mask, seed=N + d)
+    check_full(fa, case, B, H, N, d, causal, "bf16")
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,mask", [
+    (1, 2, 256, 64, False, "none"), (1, 2, 256, 64, True, "none"),
+    (1, 2, 200, 128, True, "none"), (2, 2, 300, 64, False, "padding"),
+    (1, 2, 384, 64, False, "sparse"),
+])
+def test_small_fp32(fa, B, H, N, d, causal, mask):
+    case = small_case(B, H, N, d, mask, seed=N + d + 1, dtype="fp32")
+    check_full(fa, case, B, H, N, d, causal, "fp32")
+
+
+def test_empty_rows(fa):
+    """Block-sparse rows with no visible tile: O = 0, lse = -inf, no gradient."""
+    B, H, N, d = 1, 2, 384, 64
+    bm = np.array([[0, 0, 0], [1, 1, 0], [0, 1, 1]], np.uint8)
+    case = random_case(B, H, N, d, seed=3, block_mask=bm)
+    o, lse, grads = check_full(fa, case, B, H, N, d, False, "bf16")
+    assert torch.all(o[:, :, :128] == 0)
+    assert torch.all(torch.isneginf(lse[:, :, :128]))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_causal"])
+def test_workload_tiny_fp32(fa, name):
+    w = WORKLOADS[name]
+    case = generate(w)
+    check_full(fa, case, w.B, w.H, w.N, w.d, w.causal, "fp32")
+
+
+@pytest.mark.parametrize("name", ["gpt2_causal", "bert_padding"])
+def test_workload_full(fa, name):
+    w = WORKLOADS[name]
+    case = generate(w)
+    check_full(fa, case, w.B, w.H, w.N, w.d, w.causal, "bf16")
+
+
+def test_forward_is_deterministic(fa):
+    case = random_case(1, 2, 1000, 128, seed=11)
+    t = to_device(case, "bf16")
+    o1, l1 = fa.forward(t["q"], t["k"], t["v"], 128 ** -0.5, True)
+    o2, l2 = fa.forward(t["q"], t["k"], t["v"], 128 ** -0.5, True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    assert torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------------------
+# long workloads: sampled rows (O, lse, dQ on 256 query rows of every head;
+# dK, dV on 256 key rows of the first KEY_HEADS heads of batch 0, which need
+# the oracle's statistics of every row) plus a property that holds at any size
+# ---------------------------------------------------------------------------
+
+KEY_HEADS = 2
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["long_causal_d128", "block_sparse"])
+def test_workload_sampled(fa, name):
+    w = WORKLOADS[name]
+    case = generate(w)
+    scale = w.scale
+    t = to_device(case, "bf16")
+    o, lse, (dq, dk, dv) = run(fa, t, scale, w.causal)
+    kw = dict(causal=w.causal, kv_len=case["kv_len"], block_mask=case["block_mask"])
+    rows, cols = case["rows"], case["cols"]
+    to, tl, tg = TOL["bf16"]
+    take = lambda a, r: np.take_along_axis(a, r[..., None], axis=2)
+    ro, rl = oracle.forward_rows(case["q"], case["k"], case["v"], scale, rows, **kw)
+    assert max_abs(take(f64(o), rows), ro) <= to
+    assert max_abs(np.take_along_axis(lse.cpu().numpy().astype(np.float64), rows, axis=2), rl) <= tl
+    rdq = oracle.backward_query_rows(case["q"], case["k"], case["v"], case["do"], scale, rows, **kw)
+    assert rel_fro(take(f64(dq), rows), rdq) <= tg
+    sl = (slice(0, 1), slice(0, KEY_HEADS))
+    sub = {n: case[n][sl] for n in ("q", "k", "v", "do")}
+    sub_kw = dict(kw)
+    if kw["kv_len"] is not None:
+        sub_kw["kv_len"] = kw["kv_len"][:1]
+    lse_all, d_all = oracle.row_stats(sub["q"], sub["k"], sub["v"], sub["do"], scale, **sub_kw)
+    rdk, rdv = oracle.backward_key_rows(sub["q"], sub["k"], sub["v"], sub["do"], scale,
+                                        cols[sl], lse_all, d_all, **sub_kw)
+    assert rel_fro(take(f64(dk)[sl], cols[sl]), rdk) <= tg
+    assert rel_fro(take(f64(dv)[sl], cols[sl]), rdv) <= tg
+    # the oracle's lse of every row of those heads against the GPU's
+    assert max_abs(lse.cpu().numpy().astype(np.float64)[sl], lse_all) <= tl
+    # any size: shifting every key by one vector leaves O unchanged, so the
+    # key gradients of each head sum to zero (bf16 rounding allows a little)
+    dk64 = f64(dk)
+    tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
+    per = np.linalg.norm(dk64, axis=(2, 3))
+    assert np.all(tot <= 2e-2 * per)
