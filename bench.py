@@ -1,0 +1,416 @@
+"""Benchmark: exact attention forward + backward through libfa on GB300.
+
+One step = the whole hot path over one batch: fa_fwd (O, lse), then the
+backward's three kernels (D preprocess, dK/dV/dQ kernel, dQ conversion).
+Default inputs are seeded synthetic tensors shaped like the long-context
+causal workload (B=1, H=16, N=16384, d=128, bf16, values N(0,1) x 0.5); Q, K,
+V, dO are 256 MiB together, larger than the 129 MB L2, so no flush is needed.
+
+Prints ONE JSON line (rank 0).  Metric: attention fwd+bwd TFLOP/s with the
+FLOP convention fwd = 4 B H N^2 d (halved for causal), bwd = 2.5 x fwd.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference] [--no-extras]
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only under torchrun).  Multi-GPU runs are
+independent replicas (every (batch, head) is independent; no collective).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import WORKLOADS, generate, flops  # noqa: E402
+
+METRIC = "attention fwd+bwd TFLOP/s (bf16, causal, 1 GB300) and % of dense bf16 peak"
+DEFAULT_WORKLOAD = "long_causal_d128"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def kept_fraction(block_mask):
+    if block_mask is None:
+        return None
+    return float(np.asarray(block_mask, np.float64).mean())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import exact_attention_88_gb300 as fa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOADS[args.workload]
+    case = generate(w, seed=0, samples=1)
+    to_dev = lambda n: torch.from_numpy(case[n + "_bits"].view(np.int16)).view(torch.bfloat16).to(dev)
+    q, k, v, do = (to_dev(n) for n in ("q", "k", "v", "do"))
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = w.scale
+    kv_len = None if case["kv_len"] is None else torch.from_numpy(case["kv_len"]).to(dev)
+    bmask = None if case["block_mask"] is None else torch.from_numpy(case["block_mask"]).to(dev)
+    mask = fa.make_mask(kv_len, bmask)
+    kept = kept_fraction(case["block_mask"])
+    fwd_flops, step_flops = flops(w, kept)
+
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    rows = B * H * N
+    D = ws[: rows * 4].view(torch.float32)
+    off = (rows * 4 + 255) // 256 * 256
+    dq_acc = ws[off: off + rows * d * 4].view(torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    kernels = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    ev = {n: [] for n in kernels}
+
+    def step(record):
+        def mark(name, fn):
+            if record:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ev[name].append((a, b))
+            else:
+                fn()
+        mark("fwd", lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, stream))
+        mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, dq_acc, B, H, N, d, stream))
+        mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv(q, k, v, do, lse, D, dq_acc, dk, dv, B, H, N, d,
+                                                scale, w.causal, mask, stream))
+        mark("bwd_dq_convert", lambda: fa.fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, stream))
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(False)
+    barrier()
+    code, site = fa.fa_get_device_status(stream)
+    if code != 0:
+        raise RuntimeError("device status %d at site %d during warm-up" % (code, site))
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(False)
+    t1.record(stream)
+    barrier()
+    elapsed_ms = t0.elapsed_time(t1)
+    # per-kernel pass: CUDA events on the launching stream around each launch
+    for _ in range(args.steps):
+        step(True)
+    barrier()
+    clocks = sampler.stop()
+    code, site = fa.fa_get_device_status(stream)
+    if code != 0:
+        raise RuntimeError("device status %d at site %d in the timed region" % (code, site))
+    per_kernel = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in kernels}
+
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    if rank != 0:
+        return None
+    peaks, peak_kind = measured_peaks()
+    peak = peaks["bf16_tflops"]
+    dkdv_flops = 2.5 * fwd_flops
+    achieved = dkdv_flops / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
+    fwd_achieved = fwd_flops / (per_kernel["fwd"] * 1e-3) / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) x %g, bf16)" % w.value_scale,
+        "config": {
+            "workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
+            "mask": w.mask, "kept_tile_fraction": kept, "global_batch": B * world,
+            "seq_len": N, "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs (Q,K,V,dO = %d MiB) larger than the 129 MB L2; no flush" %
+                  (4 * q.numel() * 2 >> 20),
+        },
+        "pct_of_peak": round(100.0 * (value / world) / peak, 2),
+        "kernels_ms": {n: round(t, 4) for n, t in per_kernel.items()},
+        "roofline": {
+            "kernel": "fa_bwd_dkdv (S, dP, dV, dK, dQ on tcgen05)",
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": "bf16 burst, %s (MEASURED_PEAKS.json)" % peak_kind,
+            "traffic": None,
+            "flops_per_launch": dkdv_flops,
+        },
+        "fwd_roofline": {"kernel": "fa_fwd", "achieved": round(fwd_achieved, 2),
+                         "frac": round(fwd_achieved / peak, 4), "flops_per_launch": fwd_flops},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_extras:
+        result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args)
+    return result
+
+
+def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
+    """Same metric through the public API with host buffers: pinned host inputs
+    copied in, fa_fwd + fa_bwd, results (O, lse, dQ, dK, dV) copied out, all
+    inside the timed region."""
+    B, H, N, d = w.B, w.H, w.N, w.d
+    host = {n: torch.from_numpy(case[n + "_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
+            for n in ("q", "k", "v", "do")}
+    outs = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
+            for n in ("o", "dq", "dk", "dv")}
+    lse_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dev_in = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev) for n in host}
+    o = torch.empty_like(dev_in["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    g = {n: torch.empty_like(dev_in["q"]) for n in ("dq", "dk", "dv")}
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for n in host:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        fa.fa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], o, lse, B, H, N, d, w.scale, w.causal,
+                  mask, stream)
+        fa.fa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, dev_in["do"], lse, g["dq"], g["dk"],
+                  g["dv"], ws, ws_bytes, B, H, N, d, w.scale, w.causal, mask, stream)
+        outs["o"].copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        for n in ("dq", "dk", "dv"):
+            outs[n].copy_(g[n], non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values()) + lse_h.numel() * 4
+    return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores (CPU baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, case, n_rows):
+    """Time the oracle on the last n_rows query rows of head (0, 0) (the rows
+    that see the most keys under a causal mask): O, lse, dQ of those rows and
+    their dK, dV contributions.  Returns (seconds, algorithmic FLOPs of the
+    sample under the benchmark's convention)."""
+    import oracle
+    rows = np.arange(w.N - n_rows, w.N)
+    kw = dict(causal=w.causal, kv_len=case["kv_len"], block_mask=case["block_mask"])
+    t0 = time.perf_counter()
+    oracle.row_block_forward_backward(case["q"], case["k"], case["v"], case["do"], w.scale, 0, 0,
+                                      rows, **kw)
+    sec = time.perf_counter() - t0
+    vis = oracle.visible(rows, w.N, w.causal,
+                         None if case["kv_len"] is None else int(case["kv_len"][0]),
+                         case["block_mask"], w.block)
+    fwd = 4.0 * w.d * float(vis.sum())   # Q K^T and P V over the visible pairs
+    return sec, 3.5 * fwd
+
+
+def cpu_baseline(w, case, n_rows):
+    sec, fl = oracle_sample(w, case, n_rows)
+    return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
+            "kind": "oracle",
+            "sample": "fp64 numpy oracle, fwd+bwd of the last %d query rows of head (0,0) of %s "
+                      "against all %d keys (O, lse, dQ and the rows' dK/dV contributions) in "
+                      "%.1f s; BLAS matmuls threaded over the host cores, elementwise steps "
+                      "single-threaded" % (n_rows, w.name, w.N, sec)}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    w = WORKLOADS[args.workload]
+    case = generate(w, seed=0, samples=1)
+    n_rows = args.reference_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, case, n_rows)
+    secs, fl = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = oracle_sample(w, case, n_rows)
+        secs += s
+        fl += f
+    value = fl / secs / 1e12
+    cpu = {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+           "sample": "per step: fp64 numpy oracle fwd+bwd of the last %d query rows of head "
+                     "(0,0) of %s against all %d keys" % (n_rows, w.name, w.N)}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * secs / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "mask": w.mask},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip e2e and the CPU baseline (for profiler runs)")
+    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--reference-rows", type=int, default=512)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_extras and world == 1:
+            w = WORKLOADS[args.workload]
+            case = generate(w, seed=0, samples=1)
+            res["cpu_baseline"] = cpu_baseline(w, case, args.cpu_rows)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

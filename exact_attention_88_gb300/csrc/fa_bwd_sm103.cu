@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full, qdo_full, qdo_empty, s_full, p_full, mma_done, dq_free, drain;
+  __shared__ uint64_t stats_ready[2];  // lse/D of a query tile staged (128 arrivals)
   __shared__ float s_lse2[2][128], s_D[2][128];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -105,6 +106,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(&mma_done, 1);
     mbar_init(&dq_free, 128);
     mbar_init(&drain, 1);
+    mbar_init(&stats_ready[0], 128);
+    mbar_init(&stats_ready[1], 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -209,7 +212,9 @@ __global__ void __launch_bounds__(192, 1)
         s_lse2[buf][tid] = l2;
         s_D[buf][tid] = dd;
       }
-      named_barrier(1, 128);
+      mbar_arrive(&stats_ready[buf]);
+      ok = mbar_wait_warp(&stats_ready[buf], (it >> 1) & 1, &abort_flag, p.status, 600);
+      if (!ok) break;
       ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 601);
       if (!ok) break;
       tc_fence_after();
@@ -267,7 +272,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&dq_free);
     }
     // ------------------------------------------------------------ dK, dV out
-    if (ok && !abort_flag && key < p.N) {
+    // the TMEM loads are warp-collective: every lane takes part, only the
+    // stores are limited to rows inside the sequence
+    const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
+    if (live) {
       const size_t base = (head_row0 + key) * D;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
@@ -282,15 +290,17 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = 0u;
           }
-          uint4* dst = reinterpret_cast<uint4*>(out + base + c * 32);
+          if (key < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + base + c * 32);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
-            w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
-            w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
-            w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
-            dst[g] = w;
+            for (int g = 0; g < 4; ++g) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
+              w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
+              w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
+              w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
+              dst[g] = w;
+            }
           }
         }
       }

@@ -304,7 +304,7 @@ __global__ void __launch_bounds__(192, 1)
                               p.status, 304);
         tc_fence_after();
       }
-      if (!abort_flag) {
+      if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
         const bool empty_row = !(l > 0.f);
         const float inv = empty_row ? 0.f : 1.f / l;
         const size_t base = ((size_t)bh * p.N + row) * D;
