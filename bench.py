@@ -379,8 +379,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e and the CPU baseline (for profiler runs)")
-    ap.add_argument("--cpu-rows", type=int, default=2048)
-    ap.add_argument("--reference-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
+    ap.add_argument("--reference-rows", type=int, default=2048)
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
