@@ -15,7 +15,7 @@ import os
 __all__ = [
     "FaError", "FaMask", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_fwd_fp32", "fa_bwd_fp32",
-    "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
+    "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
     "make_mask", "forward", "backward", "LIB_PATH",
     "FA_MASK_NONE", "FA_MASK_KEY_PADDING", "FA_MASK_BLOCK_SPARSE", "STATUS",
 ]
@@ -62,6 +62,7 @@ _SIGS = {
     "fa_get_device_status": [_p, ctypes.POINTER(ctypes.c_int)],
     "fa_debug_umma_gemm": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p],
     "fa_debug_wait_timeout": [ctypes.c_uint, _p],
+    "fa_bwd_noalloc": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -147,6 +148,19 @@ def fa_bwd_dkdv(q, k, v, dO, lse, D, dq_acc, dk, dv, B, H, N, d, scale, causal, 
 def fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, stream=None):
     _check(lib.fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, _stream(stream)),
            "fa_bwd_dq_convert")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20   # FA_NOALLOC_SCRATCH_BYTES
+
+
+def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, mask=None,
+                   stream=None):
+    """fa_bwd without a workspace argument, for callers that cannot allocate
+    device memory: the library's fixed scratch array is used instead (sizes
+    whose workspace exceeds NOALLOC_SCRATCH_BYTES raise FaError)."""
+    _check(lib.fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), B, H, N, d, scale, int(causal), mask,
+                              _stream(stream)), "fa_bwd_noalloc")
 
 
 def fa_status_string(code):

@@ -25,6 +25,7 @@ SOURCES = [
     "fa_bwd_aux.cu",
     "fa_fp32.cu",
     "fa_probe.cu",
+    "fa_noalloc.cu",
 ]
 HEADERS = ["fa_common.cuh", "fa_internal.h"]
 

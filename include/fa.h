@@ -129,6 +129,33 @@ fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const floa
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                       float scale, int causal, const fa_mask* mask, void* stream);
 
+/* Size of the fixed scratch array fa_bwd_noalloc works in: 32 MiB. */
+#define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* fa_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call.  fa_bwd needs a caller-allocated workspace; some
+ * callers cannot provide one, for example a plugin inside a host framework
+ * that has reserved all device memory for its own pool and does not let
+ * extensions call cudaMalloc, or latency-critical code that must avoid
+ * cudaMalloc/cudaFree because they can synchronize the whole device.  This
+ * call takes the workspace from a fixed array of FA_NOALLOC_SCRATCH_BYTES
+ * compiled into the library (every GPU that loads the library holds it until
+ * the process exits) and calls no allocator at all.
+ *   Arguments and results are those of fa_bwd without the workspace pair.
+ *   Sizes whose workspace (fa_bwd_workspace_size) exceeds
+ *   FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED.
+ *   The first call on a device looks up the array's device address (a CUDA
+ *   runtime query, done once per device with that device current); make that
+ *   first call before any stream capture.
+ *   Every call shares the one array, which keeps the previous call's
+ *   contents; each call rewrites what it needs before reading it.  Calls that
+ *   overlap on the GPU (other streams, other host threads) race on the array:
+ *   serialize them. */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                         void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 
