@@ -9,17 +9,23 @@
 //
 // One CTA owns a 128-key tile K_j, V_j of one (batch, head) and walks the
 // query tiles Q_i that can see it (causal: i >= j; block-sparse: mask[i][j]).
-// Everything is computed transposed, keys on the TMEM lanes:
-//   S^T  = K_j Q_i^T      -> TMEM [0,128)        (tcgen05, both K-major)
-//   dP^T = V_j dO_i^T     -> TMEM [128,256)
-//   P^T  = 2^(c S^T - lse2_i),  dS^T = scale P^T o (dP^T - D_i)    (warps 0-3,
-//          one key row per thread, written as bf16 to swizzled shared memory)
-//   dV  += P^T dO_i       -> TMEM [256, 256+d)   (B operand MN-major)
-//   dK  += dS^T Q_i       -> TMEM [256+d, 256+2d)
-//   dQ_i = dS K_j         -> TMEM [0, d), the same shared-memory dS^T tile
-//          read through an MN-major descriptor; warps 0-3 add it into the
-//          fp32 dq accumulator with vector reductions.
-// Roles: warps 0-3 compute, warp 4 TMA producer, warp 5 MMA issuer.
+// Everything is computed transposed, keys on the TMEM lanes.  TMEM columns:
+//   [0, d)          dV accumulator          [d, 2d)        dK accumulator
+//   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T (bf16, packed two per column)
+//   [2d+128, +128)  dP^T = V_j dO_i^T, then dQ_i = dS K_j (d columns)
+// Per query tile:
+//   MMA:   S^T, dP^T (both operands K-major in shared memory)
+//   math:  P^T = 2^(c S^T - lse2_i) back into TMEM; dS^T = scale P^T o (dP^T - D_i)
+//          as bf16 into 128-byte-swizzled shared memory
+//   MMA:   dV += P^T dO_i (A from TMEM), dK += dS^T Q_i, dQ_i = dS K_j (A = the same
+//          dS^T tile read through an MN-major descriptor)
+//   math:  dQ_i rows read out of TMEM and added into the fp32 accumulator.
+// The next tile's S^T is issued as soon as dV/dK have consumed P^T, and its
+// dP^T as soon as dQ_i has been read out; Q_i / dO_i are double-buffered.
+//
+// Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4) of
+// the read-outs; warp 16 is the TMA producer; warp 17 issues the MMAs.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -33,16 +39,21 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kSBytes = 128 * 128 * 2;  // P^T or dS^T tile, bf16
+  static constexpr int kStages = (D == 64) ? 3 : 2;  // Q / dO ring
+  static constexpr int kSBytes = 128 * 128 * 2;      // dS^T tile, bf16
   static constexpr int kOffK = 0;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffQ = kOffV + kTileBytes;
-  static constexpr int kOffDO = kOffQ + kTileBytes;
-  static constexpr int kOffP = kOffDO + kTileBytes;
-  static constexpr int kOffDS = kOffP + kSBytes;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;
+  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
+  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
   static constexpr int kSmem = kOffDS + kSBytes + 1024;
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D, kColDQ = 0;
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
+  static constexpr uint32_t kColDQ = kColDP;
+  static constexpr int kMathWarps = 16;
+  static constexpr int kMathThreads = kMathWarps * 32;
+  static constexpr int kThreads = kMathThreads + 64;
+  static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-outs
 };
 
 struct BwdParams {
@@ -71,8 +82,20 @@ struct QTileIter {
   }
 };
 
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, int n) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int g = 0; g < n / 8; ++g) {
+    uint4 w;
+    w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
+    w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
+    w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
+    w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
+    d4[g] = w;
+  }
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
@@ -80,9 +103,10 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, qdo_full, qdo_empty, s_full, p_full, mma_done, dq_free, drain;
-  __shared__ uint64_t stats_ready[2];  // lse/D of a query tile staged (128 arrivals)
-  __shared__ float s_lse2[2][128], s_D[2][128];
+  __shared__ uint64_t kv_full, s_full, p_full, acc_done, dq_full, dq_free, stats_ready, drain;
+  __shared__ uint64_t qdo_full[C::kStages], qdo_empty[C::kStages];
+  __shared__ __align__(16) float s_lse2[128];
+  __shared__ __align__(16) float s_D[128];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -99,25 +123,27 @@ __global__ void __launch_bounds__(192, 1)
 
   if (tid == 0) {
     mbar_init(&kv_full, 1);
-    mbar_init(&qdo_full, 1);
-    mbar_init(&qdo_empty, 1);
     mbar_init(&s_full, 1);
-    mbar_init(&p_full, 128);
-    mbar_init(&mma_done, 1);
-    mbar_init(&dq_free, 128);
+    mbar_init(&p_full, C::kMathThreads);
+    mbar_init(&acc_done, 1);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_free, C::kMathThreads);
+    mbar_init(&stats_ready, 128);
     mbar_init(&drain, 1);
-    mbar_init(&stats_ready[0], 128);
-    mbar_init(&stats_ready[1], 128);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&tmem_slot, C::kTmemCols);
+  if (warp == C::kMathWarps + 1) tmem_alloc(&tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 4) {
+  if (warp == C::kMathWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && iend > 0) {
       prefetch_tensormap(&tmQ);
@@ -129,141 +155,179 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_3d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, bh);
         tma_load_3d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, bh);
       }
+      int count[C::kStages] = {};
       int it = 0;
       for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-        if (!mbar_wait(&qdo_empty, (it & 1) ^ 1, &abort_flag, p.status, 401)) break;
-        mbar_expect_tx(&qdo_full, 2 * C::kTileBytes);
+        const int st = it % C::kStages;
+        if (!mbar_wait(&qdo_empty[st], ((it / C::kStages) & 1) ^ 1, &abort_flag, p.status, 401))
+          break;
+        mbar_expect_tx(&qdo_full[st], 2 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmQ, &qdo_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, i * 128, bh);
-          tma_load_3d(&tmDO, &qdo_full, smem + C::kOffDO + c * C::kChunkBytes, c * 64, i * 128, bh);
+          tma_load_3d(&tmQ, &qdo_full[st], smem + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, i * 128, bh);
+          tma_load_3d(&tmDO, &qdo_full[st],
+                      smem + C::kOffDO + st * C::kTileBytes + c * C::kChunkBytes, c * 64, i * 128, bh);
         }
+        ++count[st];
       }
       mbar_drain(&kv_full, 0);
-      if (it > 0) mbar_drain(&qdo_full, (it - 1) & 1);
+      for (int s = 0; s < C::kStages; ++s)
+        if (count[s]) mbar_drain(&qdo_full[s], (count[s] - 1) & 1);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::kMathWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && iend > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
       constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);     // dQ
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
-      const uint32_t sQ = smem_addr(smem + C::kOffQ), sDO = smem_addr(smem + C::kOffDO);
-      const uint32_t sP = smem_addr(smem + C::kOffP), sDS = smem_addr(smem + C::kOffDS);
+      const uint32_t sQ0 = smem_addr(smem + C::kOffQ), sDO0 = smem_addr(smem + C::kOffDO);
+      const uint32_t sDS = smem_addr(smem + C::kOffDS);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
-        ok = mbar_wait(&qdo_full, it & 1, &abort_flag, p.status, 502);
-        if (ok && it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 503);
+        const int st = it % C::kStages;
+        const uint32_t sQ = sQ0 + st * C::kTileBytes, sDO = sDO0 + st * C::kTileBytes;
+        ok = mbar_wait(&qdo_full[st], (it / C::kStages) & 1, &abort_flag, p.status, 502);
+        if (ok && it > 0) ok = mbar_wait(&acc_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T  (K-major operands, K dimension = d)
+        // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t koff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
           mma_ss(tmem + C::kColS, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
                  idesc_s, ks > 0);
+        }
+        if (it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 504);
+        if (!ok) break;
+        tc_fence_after();
+        // dP^T = V dO^T
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t koff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
           mma_ss(tmem + C::kColDP, sdesc_sw128(sV + koff, 16, 1024),
                  sdesc_sw128(sDO + koff, 16, 1024), idesc_s, ks > 0);
         }
         mma_commit(&s_full);
-        ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 504);
+        ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 505);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO, dK += dS^T Q   (A K-major over queries, B MN-major)
-        // dQ  = dS K                   (A = dS^T read MN-major, B = K MN-major)
+        // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed
+        // in columns [32w, 32w+16) of the S^T region), dK += dS^T Q
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t aoff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
           const uint32_t moff = ks * 2048;
           const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
-          mma_ss(tmem + C::kColDV, sdesc_sw128(sP + aoff, 16, 1024),
+          mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
                  sdesc_sw128(sDO + moff, C::kChunkBytes, 1024), idesc_acc, acc);
           mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + aoff, 16, 1024),
                  sdesc_sw128(sQ + moff, C::kChunkBytes, 1024), idesc_acc, acc);
+        }
+        mma_commit(&acc_done);
+        mma_commit(&qdo_empty[st]);
+        // dQ_i = dS K_j into the (consumed) dP^T columns
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t moff = ks * 2048;
           mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + moff, C::kChunkBytes, 1024),
                  sdesc_sw128(sK + moff, C::kChunkBytes, 1024), idesc_dq, ks > 0);
         }
-        mma_commit(&mma_done);
-        mma_commit(&qdo_empty);
+        mma_commit(&dq_full);
       }
       mma_commit(&drain);
       mbar_drain(&drain, 0);
     }
   } else {
-    // ------------------------------------------------------------ compute
-    const int key = kt * 128 + tid;  // key row of this thread
+    // ------------------------------------------------------------ math warpgroups
+    const int wg = warp >> 2;               // 0..3
+    const int tq = tid & 127;               // TMEM lane: key row (S^T) / query row (dQ)
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int key = kt * 128 + tq;
     const bool key_live = key < kv_limit;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t sP = smem_addr(smem + C::kOffP), sDS = smem_addr(smem + C::kOffDS);
+    const uint32_t sDS = smem_addr(smem + C::kOffDS);
     const size_t head_row0 = (size_t)bh * p.N;
+    const int col0 = wg * 32;               // this warpgroup's query columns
     int it = 0;
     bool ok = true;
     for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-      const int buf = it & 1;
-      {
+      // ---- per-query-row statistics of tile i into shared memory
+      if (tid < 128) {
+        if (it > 0) ok = mbar_wait(&p_full, (it - 1) & 1, &abort_flag, p.status, 600);
         const int q = i * 128 + tid;
         float l2 = INFINITY, dd = 0.f;
         if (q < p.N) {
           const float l = p.lse[head_row0 + q];
-          if (l != -INFINITY) l2 = l * kLog2e;  // empty rows keep +inf: P = 0
+          if (l != -INFINITY) l2 = l * kLog2e;  // rows with no visible key: P = 0
           dd = p.Dvec[head_row0 + q];
         }
-        s_lse2[buf][tid] = l2;
-        s_D[buf][tid] = dd;
+        s_lse2[tid] = l2;
+        s_D[tid] = dd;
+        mbar_arrive(&stats_ready);
       }
-      mbar_arrive(&stats_ready[buf]);
-      ok = mbar_wait_warp(&stats_ready[buf], (it >> 1) & 1, &abort_flag, p.status, 600);
-      if (!ok) break;
-      ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 601);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
+      if (ok) ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
       const int q0 = i * 128;
-      const bool need_causal = p.causal && (q0 < kt * 128 + 127);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {  // 32 query columns at a time
-        uint32_t rs[32], rp[32];
-        FA_TMEM_LD32_SYNC(tmem + C::kColS + lane_off + c * 32, rs);
-        FA_TMEM_LD32_SYNC(tmem + C::kColDP + lane_off + c * 32, rp);
-        uint32_t pp[16], dp[16];
+      const bool need_causal = p.causal && (q0 + col0 < kt * 128 + 127);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int qc = c * 32 + e + u;
-            float pr = ex2(fmaf(__uint_as_float(rs[e + u]), p.scale_log2, -s_lse2[buf][qc]));
-            if (!key_live || (need_causal && key > q0 + qc)) pr = 0.f;
-            pv[u] = pr;
-            dv[u] = p.scale * pr * (__uint_as_float(rp[e + u]) - s_D[buf][qc]);
-          }
-          pp[e / 2] = pack_bf16(pv[0], pv[1]);
-          dp[e / 2] = pack_bf16(dv[0], dv[1]);
-        }
+      for (int h = 0; h < 2; ++h) {  // 16 query columns at a time
+        const int c0 = col0 + h * 16;
+        uint32_t rs[16], rp[16];
+        FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
+        FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + c0, rp);
+        uint32_t pp[8], dsp[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const int col = c * 32 + g * 8;
-          const uint32_t off = (col >> 6) * C::kChunkBytes + sw128_offset(tid, col & 63);
-          st_shared_v4(sP + off, pp[4 * g], pp[4 * g + 1], pp[4 * g + 2], pp[4 * g + 3]);
-          st_shared_v4(sDS + off, dp[4 * g], dp[4 * g + 1], dp[4 * g + 2], dp[4 * g + 3]);
+          const float4 L = *reinterpret_cast<const float4*>(&s_lse2[c0 + 4 * g]);
+          const float4 Dd = *reinterpret_cast<const float4*>(&s_D[c0 + 4 * g]);
+          const float lv[4] = {L.x, L.y, L.z, L.w};
+          const float dv4[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
+          float pv[4], sv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int e = 4 * g + u;
+            float pr = ex2(fmaf(__uint_as_float(rs[e]), p.scale_log2, -lv[u]));
+            if (!key_live || (need_causal && key > q0 + c0 + e)) pr = 0.f;
+            pv[u] = pr;
+            sv[u] = p.scale * pr * (__uint_as_float(rp[e]) - dv4[u]);
+          }
+          pp[2 * g] = pack_bf16(pv[0], pv[1]);
+          pp[2 * g + 1] = pack_bf16(pv[2], pv[3]);
+          dsp[2 * g] = pack_bf16(sv[0], sv[1]);
+          dsp[2 * g + 1] = pack_bf16(sv[2], sv[3]);
         }
+        // dS^T row tq, columns c0..c0+15 (two 16-byte chunks of the swizzled tile)
+        const uint32_t off0 = (c0 >> 6) * C::kChunkBytes + sw128_offset(tq, c0 & 63);
+        const uint32_t off1 = (c0 >> 6) * C::kChunkBytes + sw128_offset(tq, (c0 + 8) & 63);
+        st_shared_v4(sDS + off0, dsp[0], dsp[1], dsp[2], dsp[3]);
+        st_shared_v4(sDS + off1, dsp[4], dsp[5], dsp[6], dsp[7]);
+        // P^T (packed bf16 pairs) over S^T columns this warp has already read
+        FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + h * 8, pp);
       }
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full);
-      ok = mbar_wait_warp(&mma_done, it & 1, &abort_flag, p.status, 602);
+      // ---- dQ_i: lanes are query rows; this warpgroup's d columns
+      ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
       tc_fence_after();
-      // dQ_i rows (lanes are query rows here) into the fp32 accumulator
-      const int q = q0 + tid;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t r[32];
-        FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + c * 32, r);
+      {
+        const int q = q0 + tq;
+        float* dst = p.dq_acc + (head_row0 + q) * D + wg * C::kDSlice;
+        uint32_t r[C::kDSlice];
+        if constexpr (C::kDSlice == 32) {
+          FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
+        } else {
+          FA_TMEM_LD16_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
+        }
         if (q < p.N) {
-          float* dst = p.dq_acc + (head_row0 + q) * D + c * 32;
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
+          for (int g = 0; g < C::kDSlice / 4; ++g)
             red_add_v4(dst + 4 * g, __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
                        __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
         }
@@ -272,37 +336,27 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive(&dq_free);
     }
     // ------------------------------------------------------------ dK, dV out
-    // the TMEM loads are warp-collective: every lane takes part, only the
-    // stores are limited to rows inside the sequence
+    // TMEM loads are warp-collective: every lane takes part; only rows inside
+    // the sequence are stored.  dq_full of the last tile (waited above) also
+    // covers the last dV / dK MMAs, which were committed before it.
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
     if (live) {
-      const size_t base = (head_row0 + key) * D;
+      const size_t base = (head_row0 + key) * D + wg * C::kDSlice;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* out = which == 0 ? p.dv : p.dk;
-        const uint32_t col0 = which == 0 ? C::kColDV : C::kColDK;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          if (it > 0) {
-            FA_TMEM_LD32_SYNC(tmem + col0 + lane_off + c * 32, r);
+        uint32_t r[C::kDSlice];
+        const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + wg * C::kDSlice;
+        if (it > 0) {
+          if constexpr (C::kDSlice == 32) {
+            FA_TMEM_LD32_SYNC(tmem + col + lane_off, r);
           } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = 0u;
+            FA_TMEM_LD16_SYNC(tmem + col + lane_off, r);
           }
-          if (key < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(out + base + c * 32);
+        } else {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
-              w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
-              w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
-              w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
-              dst[g] = w;
-            }
-          }
+          for (int e = 0; e < C::kDSlice; ++e) r[e] = 0u;
         }
+        if (key < p.N) store_row_bf16((which == 0 ? p.dv : p.dk) + base, r, C::kDSlice);
       }
     }
   }
@@ -310,7 +364,7 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == C::kMathWarps + 1) {
     __syncwarp();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -343,7 +397,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D><<<p.T * BH, 192, C::kSmem, s>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 

@@ -242,6 +242,24 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
       : "r"(taddr)                                                                               \
       : "memory")
 
+// 16-column load with its wait, and an 8-column store.
+#define FA_TMEM_LD16_SYNC(taddr, r)                                                              \
+  asm volatile(                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"   \
+      "%14,%15}, [%16];\n"                                                                        \
+      "tcgen05.wait::ld.sync.aligned;"                                                           \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15])                                                                 \
+      : "r"(taddr)                                                                               \
+      : "memory")
+
+#define FA_TMEM_ST8(taddr, r)                                                                   \
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"( \
+                   taddr),                                                                      \
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),     \
+               "r"(r[7]))
+
 #define FA_TMEM_ST16(taddr, r)                                                                  \
   asm volatile(                                                                                 \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"   \

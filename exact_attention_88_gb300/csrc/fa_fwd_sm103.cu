@@ -8,15 +8,17 @@
 // Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)").  The
 // division by l is deferred to the end, which is the same quantity.
 //
-// Roles (192 threads):
+// Roles (192 threads, two CTAs per SM so that one CTA's softmax overlaps the
+// other's MMAs):
 //   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
-//              loads S_ij from TMEM, masks, updates m and l, writes
-//              P~ = 2^(c S - m) as bf16 into shared memory, rescales O in TMEM
-//              when m grew by more than 2^8 (lazy rescale), and finally
-//              writes O / l and lse.
-//   warp 4     TMA producer: Q_i once, then K_j / V_j into a ring of stages.
+//              reads S_ij from TMEM twice (row max, then exponentials), masks,
+//              updates m and l, writes P~ = 2^(c S - m) as packed bf16 over the
+//              S columns it has read, rescales O in TMEM when m grew by more
+//              than 8 in log2 units (lazy rescale), and finally writes O / l and
+//              lse.
+//   warp 4     TMA producer: Q_i once, then K_j / V_j into rings of stages.
 //   warp 5     MMA issuer (one thread): S = Q K^T into TMEM columns [0,128),
-//              O += P V into TMEM columns [128, 128+d).
+//              O += P V into TMEM columns [128, 128+d) with P read from TMEM.
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
 #include "fa_common.cuh"
 #include "fa_internal.h"
@@ -33,15 +35,12 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;             // 64-column (128-byte) chunks
   static constexpr int kTileBytes = 128 * D * 2;     // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 128 bytes
-  static constexpr int kStages = (D == 64) ? 3 : 2;  // K/V ring depth
-  static constexpr int kPBytes = 128 * 128 * 2;      // P tile (bf16)
-  static constexpr int kPBufs = 2;
+  static constexpr int kStages = (D == 64) ? 2 : 1;  // K/V ring depth (two CTAs per SM)
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kSmem = kOffP + kPBufs * kPBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 256;              // S: [0,128), O: [128, 128+D)
+  static constexpr int kSmem = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kTmemCols = 256;              // S / P: [0,128), O: [128, 128+D)
   static constexpr int kThreads = 192;
 };
 
@@ -70,17 +69,16 @@ struct TileIter {
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, s_full, s_free, drain;
+  __shared__ uint64_t q_full, s_full, p_full, o_done, drain;
   __shared__ uint64_t k_full[C::kStages], v_full[C::kStages], k_empty[C::kStages],
       v_empty[C::kStages];
-  __shared__ uint64_t p_full[C::kPBufs], o_done[C::kPBufs];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -100,17 +98,14 @@ __global__ void __launch_bounds__(192, 1)
   if (tid == 0) {
     mbar_init(&q_full, 1);
     mbar_init(&s_full, 1);
-    mbar_init(&s_free, 128);
+    mbar_init(&p_full, 128);
+    mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_empty[s], 1);
-    }
-    for (int s = 0; s < C::kPBufs; ++s) {
-      mbar_init(&p_full[s], 128);
-      mbar_init(&o_done[s], 1);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -167,30 +162,14 @@ __global__ void __launch_bounds__(192, 1)
       const uint32_t sQ = smem_addr(smem + C::kOffQ);
       const uint32_t sK = smem_addr(smem + C::kOffK);
       const uint32_t sV = smem_addr(smem + C::kOffV);
-      const uint32_t sP = smem_addr(smem + C::kOffP);
       bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 201);
       int it = 0;
-      auto issue_pv = [&](int i) -> bool {
-        const int pb = i % C::kPBufs, st = i % C::kStages;
-        if (!mbar_wait(&p_full[pb], (i / C::kPBufs) & 1, &abort_flag, p.status, 203)) return false;
-        if (!mbar_wait(&v_full[st], (i / C::kStages) & 1, &abort_flag, p.status, 204)) return false;
-        tc_fence_after();
-        const uint32_t pbase = sP + pb * C::kPBytes;
-        const uint32_t vbase = sV + st * C::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 128 keys, 16 per MMA
-          const uint64_t ad = sdesc_sw128(pbase + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
-          mma_ss(tO, ad, bd, idesc_pv, (i > 0 || ks > 0) ? 1u : 0u);
-        }
-        mma_commit(&o_done[pb]);
-        mma_commit(&v_empty[st]);
-        return true;
-      };
       for (int j = tiles.first(); ok && j < tiles.jend; j = tiles.next(j + 1), ++it) {
         const int st = it % C::kStages;
-        ok = mbar_wait(&k_full[st], (it / C::kStages) & 1, &abort_flag, p.status, 202);
-        if (ok && it > 0) ok = mbar_wait(&s_free, (it - 1) & 1, &abort_flag, p.status, 205);
+        const uint32_t ph = (it / C::kStages) & 1;
+        ok = mbar_wait(&k_full[st], ph, &abort_flag, p.status, 202);
+        // P of the previous tile sits in the S columns until its P V is done
+        if (ok && it > 0) ok = mbar_wait(&o_done, (it - 1) & 1, &abort_flag, p.status, 203);
         if (!ok) break;
         tc_fence_after();
         const uint32_t kbase = sK + st * C::kTileBytes;
@@ -202,9 +181,19 @@ __global__ void __launch_bounds__(192, 1)
         }
         mma_commit(&s_full);
         mma_commit(&k_empty[st]);
-        if (it > 0) ok = issue_pv(it - 1);
+        ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 204);
+        if (ok) ok = mbar_wait(&v_full[st], ph, &abort_flag, p.status, 205);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t vbase = sV + st * C::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {  // 128 keys, 16 per MMA; P packed 8 columns per step
+          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
+          mma_ts(tO, tS + ks * 8, bd, idesc_pv, (it > 0 || ks > 0) ? 1u : 0u);
+        }
+        mma_commit(&o_done);
+        mma_commit(&v_empty[st]);
       }
-      if (ok && it > 0) issue_pv(it - 1);
       // all MMAs issued by this thread are complete once `drain` flips
       mma_commit(&drain);
       mbar_drain(&drain, 0);
@@ -213,7 +202,6 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ softmax
     const int row = qt * 128 + tid;  // query index of this thread
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t sP = smem_addr(smem + C::kOffP);
     float m = -INFINITY, l = 0.f;
     int it = 0;
     bool ok = true;
@@ -221,29 +209,21 @@ __global__ void __launch_bounds__(192, 1)
       ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 301);
       if (!ok) break;
       tc_fence_after();
-      float s[128];
+      const int key0 = j * 128;
+      const bool need_mask = (p.causal && (key0 + 127 > qt * 128)) || key0 + 128 > kv_limit;
+      // pass 1: row maximum of the tile
+      float tmax = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
         FA_TMEM_LD32_SYNC(tS + lane_off + c * 32, r);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[e]);
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free);
-
-      const int key0 = j * 128;
-      const bool diag = p.causal && (key0 + 127 > qt * 128);
-      if (diag || key0 + 128 > kv_limit) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int key = key0 + c;
-          if (key >= kv_limit || (p.causal && key > row)) s[c] = -INFINITY;
+        for (int e = 0; e < 32; ++e) {
+          const int key = key0 + c * 32 + e;
+          const bool dead = need_mask && (key >= kv_limit || (p.causal && key > row));
+          tmax = fmaxf(tmax, dead ? -INFINITY : __uint_as_float(r[e]));
         }
       }
-      float tmax = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) tmax = fmaxf(tmax, s[c]);
       const float m_tile = tmax * p.scale_log2;
       const float m_new = fmaxf(m, m_tile);
       const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
@@ -253,25 +233,31 @@ __global__ void __launch_bounds__(192, 1)
         m = m_new;
       }
       const float m_sub = (m == -INFINITY) ? 0.f : m;
+      // pass 2: P~ = 2^(c S - m), row sum, packed bf16 over columns already read
       float rowsum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        s[c] = ex2(fmaf(s[c], p.scale_log2, -m_sub));
-        rowsum += s[c];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        FA_TMEM_LD32_SYNC(tS + lane_off + c * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float pv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = key0 + c * 32 + e + u;
+            const bool dead = need_mask && (key >= kv_limit || (p.causal && key > row));
+            pv[u] = dead ? 0.f : ex2(fmaf(__uint_as_float(r[e + u]), p.scale_log2, -m_sub));
+            rowsum += pv[u];
+          }
+          pk[e / 2] = pack_bf16(pv[0], pv[1]);
+        }
+        FA_TMEM_ST16(tS + lane_off + c * 16, pk);
       }
       l = l * alpha + rowsum;
-
-      const int pb = it % C::kPBufs;
-      if (it >= C::kPBufs) {  // PV of the tile that last used this P buffer is done
-        ok = mbar_wait_warp(&o_done[pb], ((it / C::kPBufs) - 1) & 1, &abort_flag, p.status, 302);
-        if (!ok) break;
-      }
+      // O holds the sum up to the previous tile (its P V is complete: S of this
+      // tile was issued after it); rescale when the running max moved
       if (it > 0 && __any_sync(0xffffffffu, grow)) {
-        const int prev = it - 1;
-        ok = mbar_wait_warp(&o_done[prev % C::kPBufs], (prev / C::kPBufs) & 1, &abort_flag,
-                            p.status, 303);
-        if (!ok) break;
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -280,28 +266,16 @@ __global__ void __launch_bounds__(192, 1)
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
           FA_TMEM_ST32(tO + lane_off + c * 32, r);
         }
-        tmem_wait_st();
       }
-      // P~ (bf16) row `tid` of the K-major, 128-byte-swizzled P tile
-      const uint32_t pbase = sP + pb * C::kPBytes;
-#pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        const int col = g * 8;
-        const uint32_t addr = pbase + (col >> 6) * C::kChunkBytes + sw128_offset(tid, col & 63);
-        st_shared_v4(addr, pack_bf16(s[col], s[col + 1]), pack_bf16(s[col + 2], s[col + 3]),
-                     pack_bf16(s[col + 4], s[col + 5]), pack_bf16(s[col + 6], s[col + 7]));
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive(&p_full);
     }
     // ------------------------------------------------------------ epilogue
     if (ok) {
       bool have = it > 0;
       if (have) {
-        const int prev = it - 1;
-        have = mbar_wait_warp(&o_done[prev % C::kPBufs], (prev / C::kPBufs) & 1, &abort_flag,
-                              p.status, 304);
+        have = mbar_wait_warp(&o_done, (it - 1) & 1, &abort_flag, p.status, 304);
         tc_fence_after();
       }
       if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
