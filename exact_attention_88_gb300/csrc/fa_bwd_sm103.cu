@@ -19,13 +19,18 @@
 //          as bf16 into 128-byte-swizzled shared memory
 //   MMA:   dV += P^T dO_i (A from TMEM), dK += dS^T Q_i, dQ_i = dS K_j (A = the same
 //          dS^T tile read through an MN-major descriptor)
-//   math:  dQ_i rows read out of TMEM and added into the fp32 accumulator.
+//   math:  dQ_i read out of TMEM into a 128-byte-swizzled fp32 staging tile in
+//          shared memory, one 32-column slice per warpgroup, then added into
+//          the fp32 accumulator in global memory with one TMA bulk reduce-add
+//          per slice (line-sized reductions in L2 instead of 16-byte ones).
 // The next tile's S^T is issued as soon as dV/dK have consumed P^T, and its
-// dP^T as soon as dQ_i has been read out; Q_i / dO_i are double-buffered.
+// dP^T as soon as dQ_i has been read out.  Q_i is double-buffered (and dO_i
+// too where shared memory allows).
 //
 // Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
-// query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4) of
-// the read-outs; warp 16 is the TMA producer; warp 17 issues the MMAs.
+// query columns [32w, 32w+32) of S^T / dP^T, d columns [32w, 32w+32) of dQ
+// (when w < d/32) and d columns [w d/4, (w+1) d/4) of dK, dV; warp 16 is the
+// TMA producer; warp 17 issues the MMAs.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -39,14 +44,20 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kStages = (D == 64) ? 3 : 2;  // Q / dO ring
-  static constexpr int kSBytes = 128 * 128 * 2;      // dS^T tile, bf16
+  static constexpr int kQStages = (D == 64) ? 3 : 2;   // Q ring
+  static constexpr int kDOStages = (D == 64) ? 3 : 1;  // dO ring
+  static constexpr int kSBytes = 128 * 128 * 2;       // dS^T tile, bf16
+  static constexpr int kStageBytes = 128 * 32 * 4;     // one fp32 dQ slice (128 x 32)
+  static constexpr int kReadoutWGs = D / 32;           // warpgroups that reduce dQ
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
-  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;
-  static constexpr int kOffDS = kOffDO + kStages * kTileBytes;
-  static constexpr int kSmem = kOffDS + kSBytes + 1024;
+  static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
+  static constexpr int kOffDS = kOffDO + kDOStages * kTileBytes;
+  // dQ staging: slices 0, 1 reuse the dS^T tile (free while dQ is read out);
+  // slices 2, 3 (d = 128) have their own 32 KB
+  static constexpr int kOffStage2 = kOffDS + kSBytes;
+  static constexpr int kSmem = kOffStage2 + (kReadoutWGs > 2 ? 2 * kStageBytes : 0) + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr uint32_t kColDQ = kColDP;
@@ -55,6 +66,10 @@ struct BwdCfg {
   static constexpr int kThreads = kMathThreads + 64;
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-outs
 };
+
+__device__ __forceinline__ int stage_offset_bwd(int w, int off_ds, int off_stage2, int bytes) {
+  return w < 2 ? off_ds + w * bytes : off_stage2 + (w - 2) * bytes;
+}
 
 struct BwdParams {
   const float* lse;
@@ -98,13 +113,15 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full, s_full, p_full, acc_done, dq_full, dq_free, stats_ready, drain;
-  __shared__ uint64_t qdo_full[C::kStages], qdo_empty[C::kStages];
+  __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
+  __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
+  __shared__ uint64_t staged[4];  // a warpgroup's dQ slice is in shared memory
   __shared__ __align__(16) float s_lse2[128];
   __shared__ __align__(16) float s_D[128];
   __shared__ uint32_t tmem_slot;
@@ -130,10 +147,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&dq_free, C::kMathThreads);
     mbar_init(&stats_ready, 128);
     mbar_init(&drain, 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+    for (int s = 0; s < C::kQStages; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
     }
+    for (int s = 0; s < C::kDOStages; ++s) {
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 1);
+    }
+    for (int w = 0; w < 4; ++w) mbar_init(&staged[w], 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -155,24 +177,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_load_3d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, bh);
         tma_load_3d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, bh);
       }
-      int count[C::kStages] = {};
+      prefetch_tensormap(&tmDQ);
+      int qcount[C::kQStages] = {}, dcount[C::kDOStages] = {};
       int it = 0;
       for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-        const int st = it % C::kStages;
-        if (!mbar_wait(&qdo_empty[st], ((it / C::kStages) & 1) ^ 1, &abort_flag, p.status, 401))
+        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        if (!mbar_wait(&q_empty[qs], ((it / C::kQStages) & 1) ^ 1, &abort_flag, p.status, 401))
           break;
-        mbar_expect_tx(&qdo_full[st], 2 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_3d(&tmQ, &qdo_full[st], smem + C::kOffQ + st * C::kTileBytes + c * C::kChunkBytes,
+        mbar_expect_tx(&q_full[qs], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmQ, &q_full[qs], smem + C::kOffQ + qs * C::kTileBytes + c * C::kChunkBytes,
                       c * 64, i * 128, bh);
-          tma_load_3d(&tmDO, &qdo_full[st],
-                      smem + C::kOffDO + st * C::kTileBytes + c * C::kChunkBytes, c * 64, i * 128, bh);
-        }
-        ++count[st];
+        ++qcount[qs];
+        if (!mbar_wait(&do_empty[ds], ((it / C::kDOStages) & 1) ^ 1, &abort_flag, p.status, 402))
+          break;
+        mbar_expect_tx(&do_full[ds], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmDO, &do_full[ds],
+                      smem + C::kOffDO + ds * C::kTileBytes + c * C::kChunkBytes, c * 64, i * 128, bh);
+        ++dcount[ds];
       }
       mbar_drain(&kv_full, 0);
-      for (int s = 0; s < C::kStages; ++s)
-        if (count[s]) mbar_drain(&qdo_full[s], (count[s] - 1) & 1);
+      for (int s = 0; s < C::kQStages; ++s)
+        if (qcount[s]) mbar_drain(&q_full[s], (qcount[s] - 1) & 1);
+      for (int s = 0; s < C::kDOStages; ++s)
+        if (dcount[s]) mbar_drain(&do_full[s], (dcount[s] - 1) & 1);
     }
   } else if (warp == C::kMathWarps + 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -186,9 +215,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       bool ok = mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
-        const int st = it % C::kStages;
-        const uint32_t sQ = sQ0 + st * C::kTileBytes, sDO = sDO0 + st * C::kTileBytes;
-        ok = mbar_wait(&qdo_full[st], (it / C::kStages) & 1, &abort_flag, p.status, 502);
+        const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
+        ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
         if (ok && it > 0) ok = mbar_wait(&acc_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
         tc_fence_after();
@@ -200,6 +229,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  idesc_s, ks > 0);
         }
         if (it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 504);
+        if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
         if (!ok) break;
         tc_fence_after();
         // dP^T = V dO^T
@@ -226,7 +256,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  sdesc_sw128(sQ + moff, C::kChunkBytes, 1024), idesc_acc, acc);
         }
         mma_commit(&acc_done);
-        mma_commit(&qdo_empty[st]);
+        mma_commit(&q_empty[qs]);
+        mma_commit(&do_empty[ds]);
         // dQ_i = dS K_j into the (consumed) dP^T columns
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -312,29 +343,35 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full);
-      // ---- dQ_i: lanes are query rows; this warpgroup's d columns
+      // ---- dQ_i: lanes are query rows; warpgroup wg reduces d columns
+      // [32 wg, 32 wg + 32) through a swizzled fp32 staging slice
       ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
       tc_fence_after();
-      {
-        const int q = q0 + tq;
-        float* dst = p.dq_acc + (head_row0 + q) * D + wg * C::kDSlice;
-        uint32_t r[C::kDSlice];
-        if constexpr (C::kDSlice == 32) {
-          FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
-        } else {
-          FA_TMEM_LD16_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
-        }
-        if (q < p.N) {
+      if (wg < C::kReadoutWGs) {
+        uint8_t* stage = smem + stage_offset_bwd(wg, C::kOffDS, C::kOffStage2, C::kStageBytes);
+        uint32_t r[32];
+        FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
+        const uint32_t row_base = smem_addr(stage) + (tq >> 3) * 1024 + (tq & 7) * 128;
 #pragma unroll
-          for (int g = 0; g < C::kDSlice / 4; ++g)
-            red_add_v4(dst + 4 * g, __uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                       __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3]));
+        for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the 128-byte row, XOR-swizzled
+          st_shared_v4(row_base + ((c ^ (tq & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
+                       r[4 * c + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&staged[wg]);
+        if (tq == 0) {
+          // rows past N fall outside the tensor and are not written
+          if (mbar_wait(&staged[wg], it & 1, &abort_flag, p.status, 604)) {
+            tma_reduce_add_3d(&tmDQ, stage, wg * 32, q0, bh);
+            bulk_commit();
+            bulk_wait_read();  // the staging slice may be reused after this
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&dq_free);
     }
+    if (tq == 0) bulk_wait_all();  // reduce-adds of this warpgroup are complete
     // ------------------------------------------------------------ dK, dV out
     // TMEM loads are warp-collective: every lane takes part; only rows inside
     // the sequence are stored.  dq_full of the last tile (waited above) also
@@ -374,9 +411,10 @@ template <int D>
 cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
   const int BH = a.B * a.H;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
-      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128))
+      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128) ||
+      !encode_f32_bhnd_map(&mdq, a.dq_acc, BH, a.N, D))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.lse = a.lse;
@@ -397,7 +435,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
+  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
 

@@ -57,6 +57,10 @@ struct BwdArgs {
 // 128-byte swizzle, out-of-range rows read as zero.
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
+// Encodes a 3-D TMA descriptor over a [BH, N, d] fp32 tensor with a
+// 32-column x 128-row box and 128-byte swizzle (used for reduce-adds).
+bool encode_f32_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d);
+
 // Device address of the status block of the current device (no allocation:
 // it is a __device__ variable), or nullptr on failure.
 int* device_status();
