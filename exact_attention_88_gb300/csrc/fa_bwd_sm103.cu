@@ -13,19 +13,18 @@
 //   [0, d)          dV accumulator          [d, 2d)        dK accumulator
 //   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T (bf16, packed two per column)
 //   [2d+128, +128)  dP^T = V_j dO_i^T, then dQ_i = dS K_j (d columns)
-// Per query tile:
-//   MMA:   S^T, dP^T (both operands K-major in shared memory)
-//   math:  P^T = 2^(c S^T - lse2_i) back into TMEM; dS^T = scale P^T o (dP^T - D_i)
-//          as bf16 into 128-byte-swizzled shared memory
-//   MMA:   dV += P^T dO_i (A from TMEM), dK += dS^T Q_i, dQ_i = dS K_j (A = the same
-//          dS^T tile read through an MN-major descriptor)
-//   math:  dQ_i read out of TMEM into a 128-byte-swizzled fp32 staging tile in
-//          shared memory, one 32-column slice per warpgroup, then added into
-//          the fp32 accumulator in global memory with one TMA bulk reduce-add
-//          per slice (line-sized reductions in L2 instead of 16-byte ones).
-// The next tile's S^T is issued as soon as dV/dK have consumed P^T, and its
-// dP^T as soon as dQ_i has been read out.  Q_i is double-buffered (and dO_i
-// too where shared memory allows).
+// Per query tile, in tensor-core order:
+//   S^T, dP^T      both operands K-major in shared memory
+//   (math)         P^T = 2^(c S^T - lse2_i) back into TMEM;
+//                  dS^T = scale P^T o (dP^T - D_i) as bf16 into shared memory
+//   dV += P^T dO_i (A from TMEM)
+//   dQ_i = dS K_j  (A = the dS^T tile read through an MN-major descriptor)
+//   dK += dS^T Q_i
+// then the math warps load dQ_i from TMEM (which frees those columns for the
+// next dP^T at once), stage it as 128-byte-swizzled fp32 slices in shared
+// memory (the dS^T tile and the finished Q_i buffer) and add each slice into
+// the fp32 accumulator with a TMA bulk reduce-add.  The reduce's read of the
+// staging memory is awaited only before that memory is written again.
 //
 // Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // query columns [32w, 32w+32) of S^T / dP^T, d columns [32w, 32w+32) of dQ
@@ -45,36 +44,29 @@ struct BwdCfg {
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kChunks = D / 64;
   static constexpr int kQStages = (D == 64) ? 3 : 2;   // Q ring
-  static constexpr int kDOStages = (D == 64) ? 3 : 1;  // dO ring
+  static constexpr int kDOStages = (D == 64) ? 3 : 2;  // dO ring
   static constexpr int kSBytes = 128 * 128 * 2;       // dS^T tile, bf16
-  static constexpr int kStageBytes = 128 * 32 * 4;     // one fp32 dQ slice (128 x 32)
+  static constexpr int kSliceBytes = 128 * 32 * 4;     // one fp32 dQ slice (128 x 32)
   static constexpr int kReadoutWGs = D / 32;           // warpgroups that reduce dQ
+  static constexpr int kQStagingWGs = kReadoutWGs > 2 ? kReadoutWGs - 2 : 0;  // stage in Q_i
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
   static constexpr int kOffDS = kOffDO + kDOStages * kTileBytes;
-  // dQ staging: slices 0, 1 reuse the dS^T tile (free while dQ is read out);
-  // slices 2, 3 (d = 128) have their own 32 KB
-  static constexpr int kOffStage2 = kOffDS + kSBytes;
-  static constexpr int kSmem = kOffStage2 + (kReadoutWGs > 2 ? 2 * kStageBytes : 0) + 1024;
+  static constexpr int kSmem = kOffDS + kSBytes + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr uint32_t kColDQ = kColDP;
   static constexpr int kMathWarps = 16;
   static constexpr int kMathThreads = kMathWarps * 32;
   static constexpr int kThreads = kMathThreads + 64;
-  static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-outs
+  static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the dK / dV read-out
 };
-
-__device__ __forceinline__ int stage_offset_bwd(int w, int off_ds, int off_stage2, int bytes) {
-  return w < 2 ? off_ds + w * bytes : off_stage2 + (w - 2) * bytes;
-}
 
 struct BwdParams {
   const float* lse;
   const float* Dvec;
-  float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* kv_len;
@@ -118,12 +110,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_full, p_full, acc_done, dq_full, dq_free, stats_ready, drain;
+  __shared__ uint64_t kv_full, s_full, p_full, acc_done, dq_full, dk_done, dq_free, stats_ready,
+      stage_free, drain;
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
   __shared__ uint64_t staged[4];  // a warpgroup's dQ slice is in shared memory
-  __shared__ __align__(16) float s_lse2[128];
-  __shared__ __align__(16) float s_D[128];
+  __shared__ __align__(16) float s_nl2[128];  // -lse2 of the tile's query rows
+  __shared__ __align__(16) float s_nD[128];   // -D
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -144,12 +137,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&p_full, C::kMathThreads);
     mbar_init(&acc_done, 1);
     mbar_init(&dq_full, 1);
+    mbar_init(&dk_done, 1);
     mbar_init(&dq_free, C::kMathThreads);
     mbar_init(&stats_ready, 128);
+    mbar_init(&stage_free, C::kReadoutWGs);
     mbar_init(&drain, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
+      mbar_init(&q_empty[s], 1 + C::kQStagingWGs);  // MMA commit + staging reads done
     }
     for (int s = 0; s < C::kDOStages; ++s) {
       mbar_init(&do_full[s], 1);
@@ -172,12 +167,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmDO);
+      prefetch_tensormap(&tmDQ);
       mbar_expect_tx(&kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
         tma_load_3d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, bh);
         tma_load_3d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, bh);
       }
-      prefetch_tensormap(&tmDQ);
       int qcount[C::kQStages] = {}, dcount[C::kDOStages] = {};
       int it = 0;
       for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
@@ -218,6 +213,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
         ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
+        // P^T of the previous tile sits in the S^T columns until its dV is done
         if (ok && it > 0) ok = mbar_wait(&acc_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
         tc_fence_after();
@@ -228,6 +224,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem + C::kColS, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
                  idesc_s, ks > 0);
         }
+        // dQ of the previous tile sits in the dP^T columns until it is read out
         if (it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 504);
         if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
         if (!ok) break;
@@ -243,29 +240,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 505);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed
-        // in columns [32w, 32w+16) of the S^T region), dK += dS^T Q
+        const uint32_t acc = it > 0 ? 1u : 0u;
+        // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed in
+        // columns [32w, 32w+16) of the S^T region)
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t aoff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          const uint32_t moff = ks * 2048;
-          const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
+        for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
-                 sdesc_sw128(sDO + moff, C::kChunkBytes, 1024), idesc_acc, acc);
-          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + aoff, 16, 1024),
-                 sdesc_sw128(sQ + moff, C::kChunkBytes, 1024), idesc_acc, acc);
-        }
+                 sdesc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
         mma_commit(&acc_done);
-        mma_commit(&q_empty[qs]);
         mma_commit(&do_empty[ds]);
         // dQ_i = dS K_j into the (consumed) dP^T columns
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t moff = ks * 2048;
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + moff, C::kChunkBytes, 1024),
-                 sdesc_sw128(sK + moff, C::kChunkBytes, 1024), idesc_dq, ks > 0);
-        }
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
+                 sdesc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idesc_dq, ks > 0);
         mma_commit(&dq_full);
+        // dK += dS^T Q
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024),
+                 sdesc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
+        mma_commit(&dk_done);
+        mma_commit(&q_empty[qs]);
       }
       mma_commit(&drain);
       mbar_drain(&drain, 0);
@@ -277,33 +273,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kt * 128 + tq;
     const bool key_live = key < kv_limit;
+    const bool reducer = wg < C::kReadoutWGs;
+    const bool elected = reducer && tq == 0;
     const uint32_t sDS = smem_addr(smem + C::kOffDS);
     const size_t head_row0 = (size_t)bh * p.N;
     const int col0 = wg * 32;               // this warpgroup's query columns
-    int it = 0;
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 sc2 = make_float2(p.scale, p.scale);
+    int it = 0, prev_qs = 0;
     bool ok = true;
     for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-      // ---- per-query-row statistics of tile i into shared memory
+      const int qs = it % C::kQStages;
+      // ---- the previous tile's reduce-adds have read their staging memory
+      if (elected && it > 0) {
+        bulk_wait_read();
+        mbar_arrive(&stage_free);
+        if (wg >= 2) mbar_arrive(&q_empty[prev_qs]);
+      }
+      // ---- per-query-row statistics of tile i into shared memory (negated)
       if (tid < 128) {
         if (it > 0) ok = mbar_wait(&p_full, (it - 1) & 1, &abort_flag, p.status, 600);
         const int q = i * 128 + tid;
-        float l2 = INFINITY, dd = 0.f;
+        float nl2 = -INFINITY, nd = 0.f;
         if (q < p.N) {
           const float l = p.lse[head_row0 + q];
-          if (l != -INFINITY) l2 = l * kLog2e;  // rows with no visible key: P = 0
-          dd = p.Dvec[head_row0 + q];
+          if (l != -INFINITY) nl2 = -l * kLog2e;  // rows with no visible key: P = 0
+          nd = -p.Dvec[head_row0 + q];
         }
-        s_lse2[tid] = l2;
-        s_D[tid] = dd;
+        s_nl2[tid] = nl2;
+        s_nD[tid] = nd;
         mbar_arrive(&stats_ready);
       }
       ok = __all_sync(0xffffffffu, ok);
       if (ok) ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
+      if (ok && it > 0) ok = mbar_wait_warp(&stage_free, (it - 1) & 1, &abort_flag, p.status, 605);
       if (ok) ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
       const int q0 = i * 128;
-      const bool need_causal = p.causal && (q0 + col0 < kt * 128 + 127);
+      const bool masked = !key_live || (p.causal && key > q0 + col0);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // 16 query columns at a time
         const int c0 = col0 + h * 16;
@@ -313,23 +321,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         uint32_t pp[8], dsp[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const float4 L = *reinterpret_cast<const float4*>(&s_lse2[c0 + 4 * g]);
-          const float4 Dd = *reinterpret_cast<const float4*>(&s_D[c0 + 4 * g]);
-          const float lv[4] = {L.x, L.y, L.z, L.w};
-          const float dv4[4] = {Dd.x, Dd.y, Dd.z, Dd.w};
-          float pv[4], sv[4];
+          const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
+          const float4 Dd = *reinterpret_cast<const float4*>(&s_nD[c0 + 4 * g]);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int e = 4 * g + u;
-            float pr = ex2(fmaf(__uint_as_float(rs[e]), p.scale_log2, -lv[u]));
-            if (!key_live || (need_causal && key > q0 + c0 + e)) pr = 0.f;
-            pv[u] = pr;
-            sv[u] = p.scale * pr * (__uint_as_float(rp[e]) - dv4[u]);
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * g + 2 * u;
+            const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2,
+                                  u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
+            float2 pr = make_float2(ex2(x.x), ex2(x.y));
+            if (masked) {  // causal diagonal tiles and padded keys
+              if (!key_live || key > q0 + c0 + e) pr.x = 0.f;
+              if (!key_live || key > q0 + c0 + e + 1) pr.y = 0.f;
+            }
+            const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])),
+                                  u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y));
+            const float2 dsv = mul2(mul2(pr, sc2), t);
+            pp[2 * g + u] = pack_bf16(pr.x, pr.y);
+            dsp[2 * g + u] = pack_bf16(dsv.x, dsv.y);
           }
-          pp[2 * g] = pack_bf16(pv[0], pv[1]);
-          pp[2 * g + 1] = pack_bf16(pv[2], pv[3]);
-          dsp[2 * g] = pack_bf16(sv[0], sv[1]);
-          dsp[2 * g + 1] = pack_bf16(sv[2], sv[3]);
         }
         // dS^T row tq, columns c0..c0+15 (two 16-byte chunks of the swizzled tile)
         const uint32_t off0 = (c0 >> 6) * C::kChunkBytes + sw128_offset(tq, c0 & 63);
@@ -343,15 +352,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&p_full);
-      // ---- dQ_i: lanes are query rows; warpgroup wg reduces d columns
-      // [32 wg, 32 wg + 32) through a swizzled fp32 staging slice
+      // ---- dQ_i: lanes are query rows
       ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
       tc_fence_after();
-      if (wg < C::kReadoutWGs) {
-        uint8_t* stage = smem + stage_offset_bwd(wg, C::kOffDS, C::kOffStage2, C::kStageBytes);
-        uint32_t r[32];
-        FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
+      uint32_t r[32];
+      if (reducer) FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
+      tc_fence_before();
+      mbar_arrive(&dq_free);  // the dP^T / dQ columns may be overwritten now
+      if (reducer) {
+        // staging: slices 0, 1 in the dS^T tile, 2, 3 in the finished Q_i buffer;
+        // both are free once dK (the last reader) is done
+        ok = mbar_wait_warp(&dk_done, it & 1, &abort_flag, p.status, 604);
+        if (!ok) break;
+        uint8_t* stage = wg < 2 ? smem + C::kOffDS + wg * C::kSliceBytes
+                                : smem + C::kOffQ + qs * C::kTileBytes + (wg - 2) * C::kSliceBytes;
         const uint32_t row_base = smem_addr(stage) + (tq >> 3) * 1024 + (tq & 7) * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the 128-byte row, XOR-swizzled
@@ -359,41 +374,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                        r[4 * c + 3]);
         fence_proxy_async_smem();
         mbar_arrive(&staged[wg]);
-        if (tq == 0) {
+        if (elected && mbar_wait(&staged[wg], it & 1, &abort_flag, p.status, 606)) {
           // rows past N fall outside the tensor and are not written
-          if (mbar_wait(&staged[wg], it & 1, &abort_flag, p.status, 604)) {
-            tma_reduce_add_3d(&tmDQ, stage, wg * 32, q0, bh);
-            bulk_commit();
-            bulk_wait_read();  // the staging slice may be reused after this
-          }
+          tma_reduce_add_3d(&tmDQ, stage, wg * 32, q0, bh);
+          bulk_commit();
         }
       }
-      tc_fence_before();
-      mbar_arrive(&dq_free);
+      prev_qs = qs;
     }
-    if (tq == 0) bulk_wait_all();  // reduce-adds of this warpgroup are complete
+    if (elected) bulk_wait_all();  // this warpgroup's reduce-adds are complete
     // ------------------------------------------------------------ dK, dV out
     // TMEM loads are warp-collective: every lane takes part; only rows inside
-    // the sequence are stored.  dq_full of the last tile (waited above) also
-    // covers the last dV / dK MMAs, which were committed before it.
+    // the sequence are stored.  dk_done of the last tile (waited above by the
+    // reducing warpgroups) or dq_full (all) cover the last dV / dK MMAs.
+    if (__all_sync(0xffffffffu, ok && !abort_flag) && it > 0)
+      ok = mbar_wait_warp(&dk_done, (it - 1) & 1, &abort_flag, p.status, 607);
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
     if (live) {
+      tc_fence_after();
       const size_t base = (head_row0 + key) * D + wg * C::kDSlice;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
-        uint32_t r[C::kDSlice];
+        uint32_t rr[C::kDSlice];
         const uint32_t col = (which == 0 ? C::kColDV : C::kColDK) + wg * C::kDSlice;
         if (it > 0) {
           if constexpr (C::kDSlice == 32) {
-            FA_TMEM_LD32_SYNC(tmem + col + lane_off, r);
+            FA_TMEM_LD32_SYNC(tmem + col + lane_off, rr);
           } else {
-            FA_TMEM_LD16_SYNC(tmem + col + lane_off, r);
+            FA_TMEM_LD16_SYNC(tmem + col + lane_off, rr);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < C::kDSlice; ++e) r[e] = 0u;
+          for (int e = 0; e < C::kDSlice; ++e) rr[e] = 0u;
         }
-        if (key < p.N) store_row_bf16((which == 0 ? p.dv : p.dk) + base, r, C::kDSlice);
+        if (key < p.N) store_row_bf16((which == 0 ? p.dv : p.dk) + base, rr, C::kDSlice);
       }
     }
   }
@@ -419,7 +433,6 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.D;
-  p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;

@@ -1,24 +1,29 @@
 // Forward pass of exact attention on sm_103a tensor cores.
 //
-// One CTA computes a 128-row query tile Q_i of one (batch, head) against the
-// visible 128-key tiles K_j, V_j with the online-softmax recurrence
-// ("FlashAttention: Fast and Memory-Efficient Exact Attention with
-// IO-Awareness", summary page, "Method": block statistics m~, P~, l~ merged
-// into running m, l and the rescaled output O; blog review "From Online
-// Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)").  The
+// Each query row keeps a running max m, a running denominator l and an
+// unnormalised output O that are updated tile by tile over the visible 128-key
+// tiles K_j, V_j ("FlashAttention: Fast and Memory-Efficient Exact Attention
+// with IO-Awareness", summary page, "Method": block statistics m~, P~, l~
+// merged into the running m, l and the rescaled output; blog review "From
+// Online Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)").  The
 // division by l is deferred to the end, which is the same quantity.
 //
-// Roles (192 threads, two CTAs per SM so that one CTA's softmax overlaps the
-// other's MMAs):
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t);
-//              reads S_ij from TMEM twice (row max, then exponentials), masks,
-//              updates m and l, writes P~ = 2^(c S - m) as packed bf16 over the
-//              S columns it has read, rescales O in TMEM when m grew by more
-//              than 8 in log2 units (lazy rescale), and finally writes O / l and
-//              lse.
-//   warp 4     TMA producer: Q_i once, then K_j / V_j into rings of stages.
-//   warp 5     MMA issuer (one thread): S = Q K^T into TMEM columns [0,128),
-//              O += P V into TMEM columns [128, 128+d) with P read from TMEM.
+// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and
+// streams the key/value tiles through a shared ring.  The two tiles alternate
+// on the tensor core: while one tile's softmax runs on its warpgroup, the other
+// tile's S = Q K^T or O += P V is computed, so the tensor core has work
+// queued.  TMEM columns: S_A / P_A [0,128), O_A [128, 128+d), S_B / P_B
+// [256, 384), O_B [384, 384+d).
+//
+// Roles (320 threads):
+//   warps 0-3, 4-7  softmax of tile A, B: thread t owns row t (TMEM lane t);
+//                   reads S twice (row max, then exponentials), masks, updates
+//                   m and l, writes P~ = 2^(c S - m) as packed bf16 over the S
+//                   columns it has read, rescales O in TMEM when m grew by more
+//                   than 8 in log2 units (lazy rescale), and at the end writes
+//                   O / l and lse.
+//   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
+//   warp 9          MMA issuer (one thread).
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
 #include "fa_common.cuh"
 #include "fa_internal.h"
@@ -35,13 +40,13 @@ struct FwdCfg {
   static constexpr int kChunks = D / 64;             // 64-column (128-byte) chunks
   static constexpr int kTileBytes = 128 * D * 2;     // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 128 bytes
-  static constexpr int kStages = (D == 64) ? 2 : 1;  // K/V ring depth (two CTAs per SM)
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kStages = (D == 64) ? 3 : 2;  // K/V ring depth
+  static constexpr int kOffQ = 0;                    // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kSmem = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 256;              // S / P: [0,128), O: [128, 128+D)
-  static constexpr int kThreads = 192;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kThreads = 320;
 };
 
 struct FwdParams {
@@ -49,58 +54,139 @@ struct FwdParams {
   float* lse;
   const int32_t* kv_len;
   const uint8_t* block_mask;
-  int H, N, T, BH;
+  int H, N, T, BH, pairs;
   float scale_log2;
   int causal;
   int* status;
 };
 
-// Visible key tiles of query tile qt: 0 <= j < jend, skipping tiles the
-// block-sparse mask row drops.
-struct TileIter {
-  const uint8_t* row;  // block-mask row or nullptr
-  int jend;
-  __device__ int first() const { return next(0); }
-  __device__ int next(int j) const {
-    if (row)
-      while (j < jend && row[j] == 0) ++j;
+// Visibility of key tile j for the CTA's two query tiles.
+struct PairTiles {
+  const uint8_t* row_a;  // block-mask rows (nullptr: no block mask)
+  const uint8_t* row_b;
+  int jend_a, jend_b;    // tiles j >= jend are invisible (causal / key padding / past N)
+  __device__ bool vis_a(int j) const { return j < jend_a && (!row_a || row_a[j]); }
+  __device__ bool vis_b(int j) const { return j < jend_b && (!row_b || row_b[j]); }
+  __device__ int next(int j) const {  // next key tile visible to either tile
+    const int jend = max(jend_a, jend_b);
+    while (j < jend && !vis_a(j) && !vis_b(j)) ++j;
     return j;
   }
+  __device__ int end() const { return max(jend_a, jend_b); }
 };
 
+// Softmax of one query tile for one key tile: two passes over S in TMEM,
+// P~ written back over S as packed bf16, O rescaled when the max moved.
+// tS / tO include this warp's lane offset.
+__device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
+                                             int kv_limit, int row, bool causal, float scale_log2,
+                                             bool first, float& m, float& l) {
+  const bool need_mask = (causal && key0 + 127 > row) || key0 + 128 > kv_limit;
+  // pass 1: row maximum of the tile
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    FA_TMEM_LD32_SYNC(tS + c * 32, r);
+    if (need_mask) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int key = key0 + c * 32 + e;
+        const bool dead = key >= kv_limit || (causal && key > row);
+        tmax = fmaxf(tmax, dead ? -INFINITY : __uint_as_float(r[e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, __uint_as_float(r[e]));
+    }
+  }
+  const float m_tile = tmax * scale_log2;
+  const float m_new = fmaxf(m, m_tile);
+  const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
+  float alpha = 1.f;
+  if (grow) {
+    alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
+    m = m_new;
+  }
+  const float nm = (m == -INFINITY) ? 0.f : -m;
+  const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
+  // pass 2: P~ = 2^(c S - m), row sum, packed bf16 over columns already read
+  float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t r[32];
+    FA_TMEM_LD32_SYNC(tS + c * 32, r);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
+      float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+      if (need_mask) {
+        const int key = key0 + c * 32 + e;
+        if (key >= kv_limit || (causal && key > row)) pv.x = 0.f;
+        if (key + 1 >= kv_limit || (causal && key + 1 > row)) pv.y = 0.f;
+      }
+      sum2 = add2(sum2, pv);
+      pk[e / 2] = pack_bf16(pv.x, pv.y);
+    }
+    FA_TMEM_ST16(tS + c * 16, pk);
+  }
+  l = l * alpha + (sum2.x + sum2.y);
+  // O holds the sum up to the previous key tile (its P V is complete: this
+  // tile's S was issued after it); rescale when the running max moved
+  if (!first && __any_sync(0xffffffffu, grow)) {
+    for (int c = 0; c < ocols32; ++c) {
+      uint32_t r[32];
+      FA_TMEM_LD32_SYNC(tO + c * 32, r);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+      FA_TMEM_ST32(tO + c * 32, r);
+    }
+  }
+  tmem_wait_st();
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, s_full, p_full, o_done, drain;
+  __shared__ uint64_t q_full, drain;
+  __shared__ uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   __shared__ uint64_t k_full[C::kStages], v_full[C::kStages], k_empty[C::kStages],
       v_empty[C::kStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest query tiles first (causal rows near the end see the most keys)
+  // heaviest pairs first (causal rows near the end see the most keys)
   const int lin = blockIdx.x;
-  const int qt = p.T - 1 - lin / p.BH;
+  const int pair = p.pairs - 1 - lin / p.BH;
   const int bh = lin % p.BH;
   const int b = bh / p.H;
+  const int qa = 2 * pair, qb = 2 * pair + 1;  // query tiles; qb may be past the end
+  const bool has_b = qb < p.T;
 
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
-  int jend = (kv_limit + 127) / 128;
-  if (p.causal) jend = min(jend, qt + 1);
-  const TileIter tiles{p.block_mask ? p.block_mask + (size_t)qt * p.T : nullptr, jend};
+  const int jkv = (kv_limit + 127) / 128;
+  PairTiles tiles;
+  tiles.row_a = p.block_mask ? p.block_mask + (size_t)qa * p.T : nullptr;
+  tiles.row_b = (p.block_mask && has_b) ? p.block_mask + (size_t)qb * p.T : nullptr;
+  tiles.jend_a = p.causal ? min(jkv, qa + 1) : jkv;
+  tiles.jend_b = !has_b ? 0 : (p.causal ? min(jkv, qb + 1) : jkv);
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, 128);
-    mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&o_done[x], 1);
+    }
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
@@ -110,28 +196,31 @@ __global__ void __launch_bounds__(192, 2)
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&tmem_slot, C::kTmemCols);
+  if (warp == 9) tmem_alloc(&tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + 128;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      mbar_expect_tx(&q_full, C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qt * 128, bh);
+      mbar_expect_tx(&q_full, (has_b ? 2 : 1) * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qa * 128, bh);
+        if (has_b)
+          tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, c * 64,
+                      qb * 128, bh);
+      }
       int kcount[C::kStages] = {}, vcount[C::kStages] = {};
-      int it = 0;
+      int u = 0;
       bool ok = true;
-      for (int j = tiles.first(); j < tiles.jend && ok; j = tiles.next(j + 1), ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
+      for (int j = tiles.next(0); j < tiles.end() && ok; j = tiles.next(j + 1), ++u) {
+        const int st = u % C::kStages;
+        const uint32_t ph = (u / C::kStages) & 1;
         ok = mbar_wait(&k_empty[st], ph ^ 1, &abort_flag, p.status, 101);
         if (!ok) break;
         mbar_expect_tx(&k_full[st], C::kTileBytes);
@@ -154,7 +243,7 @@ __global__ void __launch_bounds__(192, 2)
         if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
@@ -162,36 +251,49 @@ __global__ void __launch_bounds__(192, 2)
       const uint32_t sQ = smem_addr(smem + C::kOffQ);
       const uint32_t sK = smem_addr(smem + C::kOffK);
       const uint32_t sV = smem_addr(smem + C::kOffV);
+      int cnt[2] = {0, 0};  // key tiles finished per query tile
       bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 201);
-      int it = 0;
-      for (int j = tiles.first(); ok && j < tiles.jend; j = tiles.next(j + 1), ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
+      int u = 0;
+      for (int j = tiles.next(0); ok && j < tiles.end(); j = tiles.next(j + 1), ++u) {
+        const int st = u % C::kStages;
+        const uint32_t ph = (u / C::kStages) & 1;
+        const bool vis[2] = {tiles.vis_a(j), tiles.vis_b(j)};
         ok = mbar_wait(&k_full[st], ph, &abort_flag, p.status, 202);
-        // P of the previous tile sits in the S columns until its P V is done
-        if (ok && it > 0) ok = mbar_wait(&o_done, (it - 1) & 1, &abort_flag, p.status, 203);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t kbase = sK + st * C::kTileBytes;
+        const uint32_t kbase = sK + st * C::kTileBytes, vbase = sV + st * C::kTileBytes;
+        // S_x = Q_x K_j^T for each tile that sees j (after x's previous P V:
+        // its P sits in the S columns until then)
+        for (int x = 0; ok && x < 2; ++x) {
+          if (!vis[x]) continue;
+          if (cnt[x] > 0) ok = mbar_wait(&o_done[x], (cnt[x] - 1) & 1, &abort_flag, p.status, 203 + x);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t qbase = sQ + x * C::kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(sQ + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024);
-          mma_ss(tS, ad, bd, idesc_qk, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
+            mma_ss(tmem + 256 * x, sdesc_sw128(qbase + off, 16, 1024),
+                   sdesc_sw128(kbase + off, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+          }
+          mma_commit(&s_full[x]);
         }
-        mma_commit(&s_full);
+        if (!ok) break;
         mma_commit(&k_empty[st]);
-        ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 204);
-        if (ok) ok = mbar_wait(&v_full[st], ph, &abort_flag, p.status, 205);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t vbase = sV + st * C::kTileBytes;
+        ok = mbar_wait(&v_full[st], ph, &abort_flag, p.status, 207);
+        // O_x += P_x V_j, P_x read from TMEM (packed, 8 columns per 16 keys)
+        for (int x = 0; ok && x < 2; ++x) {
+          if (!vis[x]) continue;
+          ok = mbar_wait(&p_full[x], cnt[x] & 1, &abort_flag, p.status, 205 + x);
+          if (!ok) break;
+          tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {  // 128 keys, 16 per MMA; P packed 8 columns per step
-          const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024);
-          mma_ts(tO, tS + ks * 8, bd, idesc_pv, (it > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + 256 * x + 128, tmem + 256 * x + ks * 8,
+                   sdesc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024), idesc_pv,
+                   (cnt[x] > 0 || ks > 0) ? 1u : 0u);
+          mma_commit(&o_done[x]);
+          ++cnt[x];
         }
-        mma_commit(&o_done);
+        if (!ok) break;
         mma_commit(&v_empty[st]);
       }
       // all MMAs issued by this thread are complete once `drain` flips
@@ -200,82 +302,33 @@ __global__ void __launch_bounds__(192, 2)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int row = qt * 128 + tid;  // query index of this thread
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int x = warp >> 2;  // query tile: 0 = A, 1 = B
+    const int qt = x == 0 ? qa : qb;
+    const int row = qt * 128 + (tid & 127);
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + 256 * x + lane_off, tO = tmem + 256 * x + 128 + lane_off;
     float m = -INFINITY, l = 0.f;
-    int it = 0;
+    int n = 0;
     bool ok = true;
-    for (int j = tiles.first(); j < tiles.jend; j = tiles.next(j + 1), ++it) {
-      ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 301);
-      if (!ok) break;
-      tc_fence_after();
-      const int key0 = j * 128;
-      const bool need_mask = (p.causal && (key0 + 127 > qt * 128)) || key0 + 128 > kv_limit;
-      // pass 1: row maximum of the tile
-      float tmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        FA_TMEM_LD32_SYNC(tS + lane_off + c * 32, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = key0 + c * 32 + e;
-          const bool dead = need_mask && (key >= kv_limit || (p.causal && key > row));
-          tmax = fmaxf(tmax, dead ? -INFINITY : __uint_as_float(r[e]));
-        }
+    const bool live_tile = x == 0 || has_b;
+    if (live_tile) {
+      for (int j = tiles.next(0); j < tiles.end(); j = tiles.next(j + 1)) {
+        if (!(x == 0 ? tiles.vis_a(j) : tiles.vis_b(j))) continue;
+        ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
+        if (!ok) break;
+        tc_fence_after();
+        softmax_tile(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0, p.scale_log2, n == 0, m,
+                     l);
+        tc_fence_before();
+        mbar_arrive(&p_full[x]);
+        ++n;
       }
-      const float m_tile = tmax * p.scale_log2;
-      const float m_new = fmaxf(m, m_tile);
-      const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
-      float alpha = 1.f;
-      if (grow) {
-        alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
-        m = m_new;
-      }
-      const float m_sub = (m == -INFINITY) ? 0.f : m;
-      // pass 2: P~ = 2^(c S - m), row sum, packed bf16 over columns already read
-      float rowsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        FA_TMEM_LD32_SYNC(tS + lane_off + c * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float pv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = key0 + c * 32 + e + u;
-            const bool dead = need_mask && (key >= kv_limit || (p.causal && key > row));
-            pv[u] = dead ? 0.f : ex2(fmaf(__uint_as_float(r[e + u]), p.scale_log2, -m_sub));
-            rowsum += pv[u];
-          }
-          pk[e / 2] = pack_bf16(pv[0], pv[1]);
-        }
-        FA_TMEM_ST16(tS + lane_off + c * 16, pk);
-      }
-      l = l * alpha + rowsum;
-      // O holds the sum up to the previous tile (its P V is complete: S of this
-      // tile was issued after it); rescale when the running max moved
-      if (it > 0 && __any_sync(0xffffffffu, grow)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          FA_TMEM_LD32_SYNC(tO + lane_off + c * 32, r);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          FA_TMEM_ST32(tO + lane_off + c * 32, r);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&p_full);
     }
     // ------------------------------------------------------------ epilogue
-    if (ok) {
-      bool have = it > 0;
+    if (ok && live_tile) {
+      bool have = n > 0;
       if (have) {
-        have = mbar_wait_warp(&o_done, (it - 1) & 1, &abort_flag, p.status, 304);
+        have = mbar_wait_warp(&o_done[x], (n - 1) & 1, &abort_flag, p.status, 304);
         tc_fence_after();
       }
       if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
@@ -286,7 +339,7 @@ __global__ void __launch_bounds__(192, 2)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           if (have) {
-            FA_TMEM_LD32_SYNC(tO + lane_off + c * 32, r);
+            FA_TMEM_LD32_SYNC(tO + c * 32, r);
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e) r[e] = 0u;
@@ -314,7 +367,7 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -336,6 +389,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.H = a.H;
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
+  p.pairs = (p.T + 1) / 2;
   p.BH = BH;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
@@ -343,7 +397,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.T * BH);
+  dim3 grid(p.pairs * BH);
   fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmem, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
