@@ -17,11 +17,10 @@
 //
 // Roles (320 threads):
 //   warps 0-3, 4-7  softmax of tile A, B: thread t owns row t (TMEM lane t);
-//                   reads S twice (row max, then exponentials), masks, updates
-//                   m and l, writes P~ = 2^(c S - m) as packed bf16 over the S
-//                   columns it has read, rescales O in TMEM when m grew by more
-//                   than 8 in log2 units (lazy rescale), and at the end writes
-//                   O / l and lse.
+//                   loads its 128 scores once, masks, updates m and l, writes
+//                   P~ = 2^(c S - m) as packed bf16 over the S columns,
+//                   rescales O in TMEM when m grew by more than 8 in log2 units
+//                   (lazy rescale), and at the end writes O / l and lse.
 //   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
 //   warp 9          MMA issuer (one thread).
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
@@ -75,31 +74,35 @@ struct PairTiles {
   __device__ int end() const { return max(jend_a, jend_b); }
 };
 
-// Softmax of one query tile for one key tile: two passes over S in TMEM,
-// P~ written back over S as packed bf16, O rescaled when the max moved.
-// tS / tO include this warp's lane offset.
+// Softmax of one query tile for one key tile, one TMEM pass: the thread's
+// 128 scores are loaded into registers, masked on boundary tiles, reduced to
+// the row max and exponentiated with independent accumulator chains, and P~
+// is written back over the S columns as packed bf16.  O is rescaled when the
+// max moved.  tS / tO include this warp's lane offset.
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
                                              bool first, float& m, float& l) {
-  const bool need_mask = (causal && key0 + 127 > row) || key0 + 128 > kv_limit;
-  // pass 1: row maximum of the tile
-  float tmax = -INFINITY;
+  uint32_t r[128];
+  FA_TMEM_LD128_SYNC(tS, r);
+  // keys [0, lim) of the tile are visible from this row
+  int lim = kv_limit - key0;
+  if (causal) lim = min(lim, row - key0 + 1);
+  if (lim < 128) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    FA_TMEM_LD32_SYNC(tS + c * 32, r);
-    if (need_mask) {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int key = key0 + c * 32 + e;
-        const bool dead = key >= kv_limit || (causal && key > row);
-        tmax = fmaxf(tmax, dead ? -INFINITY : __uint_as_float(r[e]));
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) tmax = fmaxf(tmax, __uint_as_float(r[e]));
-    }
+    for (int e = 0; e < 128; ++e)
+      if (e >= lim) r[e] = 0xff800000u;  // -inf
   }
+  // row max over 8 independent chains
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    float a = __uint_as_float(r[16 * k]);
+#pragma unroll
+    for (int e = 1; e < 15; e += 2)
+      a = max3(a, __uint_as_float(r[16 * k + e]), __uint_as_float(r[16 * k + e + 1]));
+    mx[k] = fmaxf(a, __uint_as_float(r[16 * k + 15]));
+  }
+  const float tmax = fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7]));
   const float m_tile = tmax * scale_log2;
   const float m_new = fmaxf(m, m_tile);
   const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
@@ -110,44 +113,40 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
   }
   const float nm = (m == -INFINITY) ? 0.f : -m;
   const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
-  // pass 2: P~ = 2^(c S - m), row sum, packed bf16 over columns already read
-  float2 sum2 = make_float2(0.f, 0.f);
+  // P~ = 2^(c S - m) with 8 independent partial sums
+  float2 acc[8];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t r[32];
-    FA_TMEM_LD32_SYNC(tS + c * 32, r);
-    uint32_t pk[16];
+  for (int k = 0; k < 8; ++k) acc[k] = make_float2(0.f, 0.f);
+  uint32_t pk[64];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
-      float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-      if (need_mask) {
-        const int key = key0 + c * 32 + e;
-        if (key >= kv_limit || (causal && key > row)) pv.x = 0.f;
-        if (key + 1 >= kv_limit || (causal && key + 1 > row)) pv.y = 0.f;
-      }
-      sum2 = add2(sum2, pv);
-      pk[e / 2] = pack_bf16(pv.x, pv.y);
-    }
-    FA_TMEM_ST16(tS + c * 16, pk);
+  for (int e = 0; e < 128; e += 2) {
+    const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
+    const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+    acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);
+    pk[e >> 1] = pack_bf16(pv.x, pv.y);
   }
-  l = l * alpha + (sum2.x + sum2.y);
+  FA_TMEM_ST32(tS, pk);
+  FA_TMEM_ST32(tS + 32, (pk + 32));
+  const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  const float2 s23 = add2(add2(acc[4], acc[5]), add2(acc[6], acc[7]));
+  const float2 st = add2(s01, s23);
+  l = l * alpha + (st.x + st.y);
   // O holds the sum up to the previous key tile (its P V is complete: this
   // tile's S was issued after it); rescale when the running max moved
   if (!first && __any_sync(0xffffffffu, grow)) {
     for (int c = 0; c < ocols32; ++c) {
-      uint32_t r[32];
-      FA_TMEM_LD32_SYNC(tO + c * 32, r);
+      uint32_t o[32];
+      FA_TMEM_LD32_SYNC(tO + c * 32, o);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-      FA_TMEM_ST32(tO + c * 32, r);
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+      FA_TMEM_ST32(tO + c * 32, o);
     }
   }
   tmem_wait_st();
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __maxnreg__(200)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
