@@ -28,9 +28,12 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_E
 
 
 class FaError(RuntimeError):
-    def __init__(self, code, where):
+    def __init__(self, code, where, detail=None):
         self.code = code
-        super().__init__("%s returned %s" % (where, STATUS.get(code, code)))
+        msg = "%s returned %s" % (where, STATUS.get(code, code))
+        if detail:
+            msg += " (%s)" % detail
+        super().__init__(msg)
 
 
 class FaMask(ctypes.Structure):
@@ -63,6 +66,7 @@ _SIGS = {
     "fa_debug_umma_gemm": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p],
     "fa_debug_wait_timeout": [ctypes.c_uint, _p],
     "fa_bwd_noalloc": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_last_cuda_error": [],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -70,6 +74,7 @@ for _name, _args in _SIGS.items():
     _fn.restype = ctypes.c_int
 lib.fa_bwd_workspace_size.restype = ctypes.c_size_t
 lib.fa_status_string.restype = ctypes.c_char_p
+lib.fa_last_cuda_error.restype = ctypes.c_char_p
 
 
 def _ptr(x):
@@ -90,7 +95,8 @@ def _stream(s):
 
 def _check(code, where):
     if code != 0:
-        raise FaError(code, where)
+        detail = lib.fa_last_cuda_error().decode() if code == 5 else None
+        raise FaError(code, where, detail)
 
 
 def make_mask(kv_len=None, block_mask=None, block_size=128):

@@ -171,7 +171,14 @@ static fa_status split_workspace(BwdArgs* a, void* ws, size_t ws_bytes) {
   return FA_OK;
 }
 
-static fa_status launched(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+// Text of the last CUDA error a call of this thread failed with.
+static thread_local const char* t_last_cuda_error = "no CUDA error";
+
+static fa_status launched(cudaError_t e) {
+  if (e == cudaSuccess) return FA_OK;
+  t_last_cuda_error = cudaGetErrorString(e);
+  return FA_ERR_CUDA;
+}
 
 extern "C" {
 
@@ -230,9 +237,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.dq = dq; a.dk = dk; a.dv = dv;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_bwd_preprocess(a, s) != cudaSuccess) return FA_ERR_CUDA;
-  if (launch_bwd_dkdv_bf16(a, s) != cudaSuccess) return FA_ERR_CUDA;
-  return launched(launch_bwd_dq_convert(a, s));
+  fa_status st2 = launched(launch_bwd_preprocess(a, s));
+  if (st2 == FA_OK) st2 = launched(launch_bwd_dkdv_bf16(a, s));
+  if (st2 == FA_OK) st2 = launched(launch_bwd_dq_convert(a, s));
+  return st2;
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H,
@@ -295,6 +303,8 @@ fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const floa
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_bwd_fp32(a, static_cast<cudaStream_t>(stream)));
 }
+
+const char* fa_last_cuda_error(void) { return t_last_cuda_error; }
 
 fa_status fa_get_device_status(void* stream, int* site) {
   if (site) *site = 0;

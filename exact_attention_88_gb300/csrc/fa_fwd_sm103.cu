@@ -17,8 +17,9 @@
 //
 // Roles (320 threads):
 //   warps 0-3, 4-7  softmax of tile A, B: thread t owns row t (TMEM lane t);
-//                   loads its 128 scores once, masks, updates m and l, writes
-//                   P~ = 2^(c S - m) as packed bf16 over the S columns,
+//                   reads its 128 scores (max, then exponentials), masks,
+//                   updates m and l, writes P~ = 2^(c S - m) as packed bf16
+//                   over the S columns,
 //                   rescales O in TMEM when m grew by more than 8 in log2 units
 //                   (lazy rescale), and at the end writes O / l and lse.
 //   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
@@ -74,35 +75,50 @@ struct PairTiles {
   __device__ int end() const { return max(jend_a, jend_b); }
 };
 
-// Softmax of one query tile for one key tile, one TMEM pass: the thread's
-// 128 scores are loaded into registers, masked on boundary tiles, reduced to
-// the row max and exponentiated with independent accumulator chains, and P~
-// is written back over the S columns as packed bf16.  O is rescaled when the
-// max moved.  tS / tO include this warp's lane offset.
+// Softmax of one query tile for one key tile.  The row max is taken over the
+// thread's 128 scores (two 64-column TMEM loads, eight independent 3-input max
+// chains); the scores are then reloaded 64 at a time (a TMEM load costs a few
+// tens of cycles), exponentiated with packed fp32x2 arithmetic and eight
+// independent partial sums, and P~ is written back over the S columns as
+// packed bf16.  Boundary tiles (causal diagonal, key padding, the end of the
+// sequence) mask invisible keys to -inf.  O is rescaled when the max moved.
+// tS / tO include this warp's lane offset.
+__device__ __forceinline__ void mask_tail(uint32_t* r, int lim) {  // keys e >= lim are invisible
+#pragma unroll
+  for (int e = 0; e < 64; ++e)
+    if (e >= lim) r[e] = 0xff800000u;  // -inf
+}
+
+__device__ __forceinline__ float max64(const uint32_t* r) {
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    mx[k] = fmaxf(max3(__uint_as_float(r[8 * k]), __uint_as_float(r[8 * k + 1]),
+                       __uint_as_float(r[8 * k + 2])),
+                  max3(__uint_as_float(r[8 * k + 3]), max3(__uint_as_float(r[8 * k + 4]),
+                                                           __uint_as_float(r[8 * k + 5]),
+                                                           __uint_as_float(r[8 * k + 6])),
+                       __uint_as_float(r[8 * k + 7])));
+  return fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7]));
+}
+
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
                                              bool first, float& m, float& l) {
-  uint32_t r[128];
-  FA_TMEM_LD128_SYNC(tS, r);
   // keys [0, lim) of the tile are visible from this row
   int lim = kv_limit - key0;
   if (causal) lim = min(lim, row - key0 + 1);
-  if (lim < 128) {
-#pragma unroll
-    for (int e = 0; e < 128; ++e)
-      if (e >= lim) r[e] = 0xff800000u;  // -inf
+  const bool partial = lim < 128;
+  float tmax;
+  {
+    uint32_t r[64];
+    FA_TMEM_LD64_SYNC(tS, r);
+    if (partial) mask_tail(r, lim);
+    tmax = max64(r);
+    FA_TMEM_LD64_SYNC(tS + 64, r);
+    if (partial) mask_tail(r, lim - 64);
+    tmax = fmaxf(tmax, max64(r));
   }
-  // row max over 8 independent chains
-  float mx[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float a = __uint_as_float(r[16 * k]);
-#pragma unroll
-    for (int e = 1; e < 15; e += 2)
-      a = max3(a, __uint_as_float(r[16 * k + e]), __uint_as_float(r[16 * k + e + 1]));
-    mx[k] = fmaxf(a, __uint_as_float(r[16 * k + 15]));
-  }
-  const float tmax = fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7]));
   const float m_tile = tmax * scale_log2;
   const float m_new = fmaxf(m, m_tile);
   const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
@@ -113,20 +129,26 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
   }
   const float nm = (m == -INFINITY) ? 0.f : -m;
   const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
-  // P~ = 2^(c S - m) with 8 independent partial sums
   float2 acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = make_float2(0.f, 0.f);
-  uint32_t pk[64];
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint32_t r[64];
+    FA_TMEM_LD64_SYNC(tS + 64 * half, r);
+    if (partial) mask_tail(r, lim - 64 * half);
+    uint32_t pk[32];
 #pragma unroll
-  for (int e = 0; e < 128; e += 2) {
-    const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
-    const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-    acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);
-    pk[e >> 1] = pack_bf16(pv.x, pv.y);
+    for (int e = 0; e < 64; e += 2) {
+      const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
+      const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+      acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);
+      pk[e >> 1] = pack_bf16(pv.x, pv.y);
+    }
+    // packed P of keys [64 half, 64 half + 64) over S columns [32 half, 32 half + 32),
+    // which this thread has already read
+    FA_TMEM_ST32(tS + 32 * half, pk);
   }
-  FA_TMEM_ST32(tS, pk);
-  FA_TMEM_ST32(tS + 32, (pk + 32));
   const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
   const float2 s23 = add2(add2(acc[4], acc[5]), add2(acc[6], acc[7]));
   const float2 st = add2(s01, s23);
@@ -146,7 +168,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;

@@ -159,6 +159,10 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 
+/* Text of the CUDA error behind the last FA_ERR_CUDA that a launching call
+ * of the calling thread returned ("no CUDA error" if none).  Static string. */
+const char* fa_last_cuda_error(void);
+
 /* Synchronizes `stream`, then reports and clears the device-side status that
  * the kernels raise when a wait inside them gives up (FA_ERR_TIMEOUT), or
  * FA_ERR_CUDA if the stream reports an error.  FA_OK otherwise.  If site is
