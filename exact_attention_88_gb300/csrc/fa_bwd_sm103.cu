@@ -11,15 +11,17 @@
 // query tiles Q_i that can see it (causal: i >= j; block-sparse: mask[i][j]).
 // Everything is computed transposed, keys on the TMEM lanes.  TMEM columns:
 //   [0, d)          dV accumulator          [d, 2d)        dK accumulator
-//   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T (bf16, packed two per column)
+//   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T and dS^T (bf16, packed two per
+//                   column: warpgroup w's P^T in [32w, 32w+16), dS^T in
+//                   [32w+16, 32w+32))
 //   [2d+128, +128)  dP^T = V_j dO_i^T, then dQ_i = dS K_j (d columns)
 // Per query tile, in tensor-core order:
 //   S^T, dP^T      both operands K-major in shared memory
-//   (math)         P^T = 2^(c S^T - lse2_i) back into TMEM;
-//                  dS^T = scale P^T o (dP^T - D_i) as bf16 into shared memory
+//   (math)         P^T = 2^(c S^T - lse2_i) and dS^T = scale P^T o (dP^T - D_i)
+//                  back into TMEM; dS^T also as bf16 into shared memory
 //   dV += P^T dO_i (A from TMEM)
-//   dQ_i = dS K_j  (A = the dS^T tile read through an MN-major descriptor)
-//   dK += dS^T Q_i
+//   dQ_i = dS K_j  (A = the dS^T tile in shared memory, read MN-major)
+//   dK += dS^T Q_i (A from TMEM)
 // then the math warps load dQ_i from TMEM (which frees those columns for the
 // next dP^T at once), stage it as 128-byte-swizzled fp32 slices in shared
 // memory (the dS^T tile and the finished Q_i buffer) and add each slice into
@@ -255,10 +257,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
                  sdesc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idesc_dq, ks > 0);
         mma_commit(&dq_full);
-        // dK += dS^T Q
+        // dK += dS^T Q (dS^T in TMEM, packed in columns [32w+16, 32w+32))
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + C::kColDK, sdesc_sw128(sDS + (ks >> 2) * C::kChunkBytes + (ks & 3) * 32, 16, 1024),
+          mma_ts(tmem + C::kColDK, tmem + C::kColS + 32 * (ks >> 1) + 16 + 8 * (ks & 1),
                  sdesc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
         mma_commit(&dk_done);
         mma_commit(&q_empty[qs]);
@@ -312,42 +314,65 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_after();
       const int q0 = i * 128;
       const bool masked = !key_live || (p.causal && key > q0 + col0);
+      // P^T and dS^T for the warpgroup's 32 columns, 16 at a time.  Packed P^T of
+      // half h goes over S^T columns [col0 + 8h, col0 + 8h + 8) (read in half 0);
+      // packed dS^T over [col0 + 16, col0 + 32), written once half 1 is read.
+      uint32_t dsp[16];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {  // 16 query columns at a time
-        const int c0 = col0 + h * 16;
-        uint32_t rs[16], rp[16];
-        FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = col0 + 16 * h;
+        float pf[16];
+        {
+          uint32_t rs[16];
+          FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int e = 4 * g + 2 * u;
+              const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])),
+                                    c2, u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
+              pf[e] = ex2(x.x);
+              pf[e + 1] = ex2(x.y);
+            }
+          }
+        }
+        if (masked) {  // causal diagonal tiles and padded keys
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (!key_live || key > q0 + c0 + e) pf[e] = 0.f;
+        }
+        {
+          uint32_t pp[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) pp[e / 2] = pack_bf16(pf[e], pf[e + 1]);
+          FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + 8 * h, pp);
+        }
+        uint32_t rp[16];
         FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + c0, rp);
-        uint32_t pp[8], dsp[8];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
           const float4 Dd = *reinterpret_cast<const float4*>(&s_nD[c0 + 4 * g]);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 4 * g + 2 * u;
-            const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2,
-                                  u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
-            float2 pr = make_float2(ex2(x.x), ex2(x.y));
-            if (masked) {  // causal diagonal tiles and padded keys
-              if (!key_live || key > q0 + c0 + e) pr.x = 0.f;
-              if (!key_live || key > q0 + c0 + e + 1) pr.y = 0.f;
-            }
             const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])),
                                   u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y));
-            const float2 dsv = mul2(mul2(pr, sc2), t);
-            pp[2 * g + u] = pack_bf16(pr.x, pr.y);
-            dsp[2 * g + u] = pack_bf16(dsv.x, dsv.y);
+            const float2 dsv = mul2(mul2(make_float2(pf[e], pf[e + 1]), sc2), t);
+            dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
           }
         }
         // dS^T row tq, columns c0..c0+15 (two 16-byte chunks of the swizzled tile)
-        const uint32_t off0 = (c0 >> 6) * C::kChunkBytes + sw128_offset(tq, c0 & 63);
-        const uint32_t off1 = (c0 >> 6) * C::kChunkBytes + sw128_offset(tq, (c0 + 8) & 63);
-        st_shared_v4(sDS + off0, dsp[0], dsp[1], dsp[2], dsp[3]);
-        st_shared_v4(sDS + off1, dsp[4], dsp[5], dsp[6], dsp[7]);
-        // P^T (packed bf16 pairs) over S^T columns this warp has already read
-        FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + h * 8, pp);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          const int c = c0 + 8 * g;
+          st_shared_v4(sDS + (c >> 6) * C::kChunkBytes + sw128_offset(tq, c & 63),
+                       dsp[8 * h + 4 * g], dsp[8 * h + 4 * g + 1], dsp[8 * h + 4 * g + 2],
+                       dsp[8 * h + 4 * g + 3]);
+        }
       }
+      FA_TMEM_ST16(tmem + C::kColS + lane_off + col0 + 16, dsp);
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
