@@ -15,15 +15,16 @@
 //                   column: warpgroup w's P^T in [32w, 32w+16), dS^T in
 //                   [32w+16, 32w+32))
 //   [2d+128, +128)  dP^T = V_j dO_i^T, then dQ_i = dS K_j (d columns)
-// Per query tile, in tensor-core order:
-//   S^T, dP^T      both operands K-major in shared memory
-//   (math)         P^T = 2^(c S^T - lse2_i) and dS^T = scale P^T o (dP^T - D_i)
-//                  back into TMEM; dS^T also as bf16 into shared memory
-//   dV += P^T dO_i (A from TMEM)
-//   dQ_i = dS K_j  (A = the dS^T tile in shared memory, read MN-major)
-//   dK += dS^T Q_i (A from TMEM)
-// then the math warps load dQ_i from TMEM (which frees those columns for the
-// next dP^T at once), stage it as 128-byte-swizzled fp32 slices in shared
+// Per query tile, in tensor-core order, with the math overlapping:
+//   S^T            both operands K-major in shared memory
+//   dP^T           (meanwhile the math computes P^T = 2^(c S^T - lse2_i) into TMEM)
+//   dV += P^T dO_i A from TMEM (meanwhile the math computes
+//                  dS^T = scale P^T o (dP^T - D_i) into TMEM and shared memory)
+//   dK += dS^T Q_i A from TMEM
+//   dQ_i = dS K_j  A = the dS^T tile in shared memory, read MN-major
+// The next tile's S^T waits only for dK (the last reader of the S^T columns).
+// The math warps load dQ_i from TMEM (which frees those columns for the next
+// dP^T at once), stage it as 128-byte-swizzled fp32 slices in shared
 // memory (the dS^T tile and the finished Q_i buffer) and add each slice into
 // the fp32 accumulator with a TMA bulk reduce-add.  The reduce's read of the
 // staging memory is awaited only before that memory is written again.
@@ -112,8 +113,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_full, p_full, acc_done, dq_full, dk_done, dq_free, stats_ready,
-      stage_free, drain;
+  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, dq_full, dk_done, dq_free,
+      stats_ready, stage_free, drain;
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
   __shared__ uint64_t staged[4];  // a warpgroup's dQ slice is in shared memory
@@ -135,9 +136,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&kv_full, 1);
-    mbar_init(&s_full, 1);
-    mbar_init(&p_full, C::kMathThreads);
-    mbar_init(&acc_done, 1);
+    mbar_init(&s_ready, 1);
+    mbar_init(&dp_ready, 1);
+    mbar_init(&p_ready, C::kMathThreads);
+    mbar_init(&ds_ready, C::kMathThreads);
     mbar_init(&dq_full, 1);
     mbar_init(&dk_done, 1);
     mbar_init(&dq_free, C::kMathThreads);
@@ -215,8 +217,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
         ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
-        // P^T of the previous tile sits in the S^T columns until its dV is done
-        if (ok && it > 0) ok = mbar_wait(&acc_done, (it - 1) & 1, &abort_flag, p.status, 503);
+        // P^T / dS^T of the previous tile sit in the S^T columns until dK is done
+        if (ok && it > 0) ok = mbar_wait(&dk_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
         tc_fence_after();
         // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
@@ -226,6 +228,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem + C::kColS, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
                  idesc_s, ks > 0);
         }
+        mma_commit(&s_ready);
         // dQ of the previous tile sits in the dP^T columns until it is read out
         if (it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 504);
         if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
@@ -238,8 +241,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem + C::kColDP, sdesc_sw128(sV + koff, 16, 1024),
                  sdesc_sw128(sDO + koff, 16, 1024), idesc_s, ks > 0);
         }
-        mma_commit(&s_full);
-        ok = mbar_wait(&p_full, it & 1, &abort_flag, p.status, 505);
+        mma_commit(&dp_ready);
+        ok = mbar_wait(&p_ready, it & 1, &abort_flag, p.status, 505);
         if (!ok) break;
         tc_fence_after();
         const uint32_t acc = it > 0 ? 1u : 0u;
@@ -249,14 +252,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
                  sdesc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
-        mma_commit(&acc_done);
         mma_commit(&do_empty[ds]);
-        // dQ_i = dS K_j into the (consumed) dP^T columns
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
-                 sdesc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idesc_dq, ks > 0);
-        mma_commit(&dq_full);
+        ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
+        if (!ok) break;
+        tc_fence_after();
         // dK += dS^T Q (dS^T in TMEM, packed in columns [32w+16, 32w+32))
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
@@ -264,6 +263,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  sdesc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
         mma_commit(&dk_done);
         mma_commit(&q_empty[qs]);
+        // dQ_i = dS K_j into the (consumed) dP^T columns
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
+                 sdesc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idesc_dq, ks > 0);
+        mma_commit(&dq_full);
       }
       mma_commit(&drain);
       mbar_drain(&drain, 0);
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       // ---- per-query-row statistics of tile i into shared memory (negated)
       if (tid < 128) {
-        if (it > 0) ok = mbar_wait(&p_full, (it - 1) & 1, &abort_flag, p.status, 600);
+        if (it > 0) ok = mbar_wait(&ds_ready, (it - 1) & 1, &abort_flag, p.status, 600);
         const int q = i * 128 + tid;
         float nl2 = -INFINITY, nd = 0.f;
         if (q < p.N) {
@@ -309,46 +314,54 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (ok) ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
       if (ok && it > 0) ok = mbar_wait_warp(&stage_free, (it - 1) & 1, &abort_flag, p.status, 605);
-      if (ok) ok = mbar_wait_warp(&s_full, it & 1, &abort_flag, p.status, 602);
+      if (ok) ok = mbar_wait_warp(&s_ready, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
       const int q0 = i * 128;
       const bool masked = !key_live || (p.causal && key > q0 + col0);
-      // P^T and dS^T for the warpgroup's 32 columns, 16 at a time.  Packed P^T of
-      // half h goes over S^T columns [col0 + 8h, col0 + 8h + 8) (read in half 0);
-      // packed dS^T over [col0 + 16, col0 + 32), written once half 1 is read.
-      uint32_t dsp[16];
+      // ---- P^T for the warpgroup's 32 columns (while dP^T is computed); packed
+      // P^T of half h goes over S^T columns [col0 + 8h, col0 + 8h + 8), which
+      // were read in half 0
+      float pf[32];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c0 = col0 + 16 * h;
-        float pf[16];
-        {
-          uint32_t rs[16];
-          FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
+        uint32_t rs[16];
+        FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
+        for (int g = 0; g < 4; ++g) {
+          const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int e = 4 * g + 2 * u;
-              const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])),
-                                    c2, u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
-              pf[e] = ex2(x.x);
-              pf[e + 1] = ex2(x.y);
-            }
+          for (int u = 0; u < 2; ++u) {
+            const int e = 4 * g + 2 * u;
+            const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])),
+                                  c2, u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
+            pf[16 * h + e] = ex2(x.x);
+            pf[16 * h + e + 1] = ex2(x.y);
           }
         }
         if (masked) {  // causal diagonal tiles and padded keys
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            if (!key_live || key > q0 + c0 + e) pf[e] = 0.f;
+            if (!key_live || key > q0 + c0 + e) pf[16 * h + e] = 0.f;
         }
-        {
-          uint32_t pp[8];
+        uint32_t pp[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) pp[e / 2] = pack_bf16(pf[e], pf[e + 1]);
-          FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + 8 * h, pp);
-        }
+        for (int e = 0; e < 16; e += 2) pp[e / 2] = pack_bf16(pf[16 * h + e], pf[16 * h + e + 1]);
+        FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + 8 * h, pp);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_ready);
+      // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): bf16 into the
+      // swizzled shared-memory tile and packed over S^T columns [col0 + 16, col0 + 32)
+      ok = mbar_wait_warp(&dp_ready, it & 1, &abort_flag, p.status, 608);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dsp[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = col0 + 16 * h;
         uint32_t rp[16];
         FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + c0, rp);
 #pragma unroll
@@ -359,11 +372,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const int e = 4 * g + 2 * u;
             const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])),
                                   u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y));
-            const float2 dsv = mul2(mul2(make_float2(pf[e], pf[e + 1]), sc2), t);
+            const float2 dsv = mul2(mul2(make_float2(pf[16 * h + e], pf[16 * h + e + 1]), sc2), t);
             dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
           }
         }
-        // dS^T row tq, columns c0..c0+15 (two 16-byte chunks of the swizzled tile)
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
           const int c = c0 + 8 * g;
@@ -376,7 +388,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full);
+      mbar_arrive(&ds_ready);
       // ---- dQ_i: lanes are query rows
       ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
@@ -386,8 +398,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tc_fence_before();
       mbar_arrive(&dq_free);  // the dP^T / dQ columns may be overwritten now
       if (reducer) {
-        // staging: slices 0, 1 in the dS^T tile, 2, 3 in the finished Q_i buffer;
-        // both are free once dK (the last reader) is done
+        // staging: slices 0, 1 in the dS^T tile (dQ, its last reader, is done),
+        // 2, 3 in the finished Q_i buffer (dK, its last reader, is done)
         ok = mbar_wait_warp(&dk_done, it & 1, &abort_flag, p.status, 604);
         if (!ok) break;
         uint8_t* stage = wg < 2 ? smem + C::kOffDS + wg * C::kSliceBytes
