@@ -87,18 +87,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Same, for a whole warp: lane 0 polls (so a waiting warp issues one probe
-// per round, not 32) and broadcasts the outcome; the warp agrees on it so that
-// the .sync.aligned tcgen05 instructions that follow stay convergent.  The
-// phase completion that lane 0 observed orders the other lanes' later reads
-// as well, since the warp synchronises on the broadcast.
+// Same, for all 32 lanes of a warp; the warp agrees on the outcome so that
+// the .sync.aligned tcgen05 instructions that follow stay convergent.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile int* abort_flag, int* status, int site) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort_flag, status, site) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();  // memory ordering among the lanes after lane 0's acquire
-  return ok != 0;
+  bool ok = mbar_wait(bar, parity, abort_flag, status, site);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Teardown wait: ignores the abort flag, shorter limit, never reports.
