@@ -289,31 +289,34 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const float2 sc2 = make_float2(p.scale, p.scale);
     int it = 0, prev_qs = 0;
     bool ok = true;
+    // Statistics of a query tile, negated, as a thread of the first warpgroup
+    // holds them between the global load and the shared-memory store.
+    struct RowStats {
+      float nl2, nd;
+    };
+    auto load_stats = [&](int qt) {
+      RowStats st{-INFINITY, 0.f};
+      const int q = qt * 128 + tid;
+      if (qt < iend && q < p.N) {
+        const float l = p.lse[head_row0 + q];
+        if (l != -INFINITY) st.nl2 = -l * kLog2e;  // rows with no visible key: P = 0
+        st.nd = -p.Dvec[head_row0 + q];
+      }
+      return st;
+    };
+    if (tid < 128 && iend > 0) {
+      const RowStats st = load_stats(qtiles.first());
+      s_nl2[tid] = st.nl2;
+      s_nD[tid] = st.nd;
+      mbar_arrive(&stats_ready);
+    }
     for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
       const int qs = it % C::kQStages;
-      // ---- the previous tile's reduce-adds have read their staging memory
-      if (elected && it > 0) {
-        bulk_wait_read();
-        mbar_arrive(&stage_free);
-        if (wg >= 2) mbar_arrive(&q_empty[prev_qs]);
-      }
-      // ---- per-query-row statistics of tile i into shared memory (negated)
-      if (tid < 128) {
-        if (it > 0) ok = mbar_wait(&ds_ready, (it - 1) & 1, &abort_flag, p.status, 600);
-        const int q = i * 128 + tid;
-        float nl2 = -INFINITY, nd = 0.f;
-        if (q < p.N) {
-          const float l = p.lse[head_row0 + q];
-          if (l != -INFINITY) nl2 = -l * kLog2e;  // rows with no visible key: P = 0
-          nd = -p.Dvec[head_row0 + q];
-        }
-        s_nl2[tid] = nl2;
-        s_nD[tid] = nd;
-        mbar_arrive(&stats_ready);
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
-      if (ok && it > 0) ok = mbar_wait_warp(&stage_free, (it - 1) & 1, &abort_flag, p.status, 605);
+      // ---- the next tile's statistics: loaded now, stored once every math
+      // thread is past this tile's dS (the loads' latency hides behind the MMAs)
+      RowStats next_st{};
+      if (tid < 128) next_st = load_stats(qtiles.next(i + 1));
+      ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
       if (ok) ok = mbar_wait_warp(&s_ready, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
@@ -353,6 +356,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_ready);
+      // ---- the previous tile's reduce-adds have read their staging memory (the
+      // dS^T tile and Q buffer written below): awaited only now, after P^T
+      if (elected && it > 0) {
+        bulk_wait_read();
+        mbar_arrive(&stage_free);
+        if (wg >= 2) mbar_arrive(&q_empty[prev_qs]);
+      }
       // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): bf16 into the
       // swizzled shared-memory tile and packed over S^T columns [col0 + 16, col0 + 32)
       ok = mbar_wait_warp(&dp_ready, it & 1, &abort_flag, p.status, 608);
@@ -376,19 +386,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
           }
         }
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-          const int c = c0 + 8 * g;
-          st_shared_v4(sDS + (c >> 6) * C::kChunkBytes + sw128_offset(tq, c & 63),
-                       dsp[8 * h + 4 * g], dsp[8 * h + 4 * g + 1], dsp[8 * h + 4 * g + 2],
-                       dsp[8 * h + 4 * g + 3]);
-        }
       }
       FA_TMEM_ST16(tmem + C::kColS + lane_off + col0 + 16, dsp);
+      if (it > 0 && !mbar_wait_warp(&stage_free, (it - 1) & 1, &abort_flag, p.status, 605)) break;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int c = col0 + 8 * g;
+        st_shared_v4(sDS + (c >> 6) * C::kChunkBytes + sw128_offset(tq, c & 63), dsp[4 * g],
+                     dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
+      }
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&ds_ready);
+      // ---- the next tile's statistics replace this tile's once every math
+      // thread is past its last read of them (ds_ready complete)
+      if (tid < 128) {
+        if (mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 600)) {
+          s_nl2[tid] = next_st.nl2;
+          s_nD[tid] = next_st.nd;
+          mbar_arrive(&stats_ready);
+        } else {
+          ok = false;
+        }
+      }
+      if (!__all_sync(0xffffffffu, ok)) break;
       // ---- dQ_i: lanes are query rows
       ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
