@@ -21,18 +21,19 @@
 //   dV += P^T dO_i A from TMEM (meanwhile the math computes
 //                  dS^T = scale P^T o (dP^T - D_i) into TMEM and shared memory)
 //   dK += dS^T Q_i A from TMEM
-//   dQ_i = dS K_j  A = the dS^T tile in shared memory, read MN-major
+//   dQ_i^T = K_j^T dS^T   both operands MN-major in shared memory (K_j and the
+//                  dS^T tile); M = 128 rows of d (for d = 64 the upper 64 rows
+//                  read past K_j and are never used)
 // The next tile's S^T waits only for dK (the last reader of the S^T columns).
-// The math warps load dQ_i from TMEM (which frees those columns for the next
-// dP^T at once), stage it as 128-byte-swizzled fp32 slices in shared
-// memory (the dS^T tile and the finished Q_i buffer) and add each slice into
-// the fp32 accumulator with a TMA bulk reduce-add.  The reduce's read of the
-// staging memory is awaited only before that memory is written again.
+// The math warps load dQ_i^T from TMEM (which frees those columns for the
+// next dP^T at once): a warp holds 32 consecutive d columns of 32 query rows,
+// so each fp32 atomic add it issues covers 128 contiguous bytes of one row of
+// the dQ accumulator -- no shared-memory staging, no bulk reduce.
 //
 // Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
-// query columns [32w, 32w+32) of S^T / dP^T, d columns [32w, 32w+32) of dQ
-// (when w < d/32) and d columns [w d/4, (w+1) d/4) of dK, dV; warp 16 is the
-// TMA producer; warp 17 issues the MMAs.
+// query columns [32w, 32w+32) of S^T / dP^T / dQ^T and d columns
+// [w d/4, (w+1) d/4) of dK, dV; warp 16 is the TMA producer; warp 17 issues
+// the MMAs.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -48,10 +49,8 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kQStages = (D == 64) ? 3 : 2;   // Q ring
   static constexpr int kDOStages = (D == 64) ? 3 : 2;  // dO ring
+  static constexpr int kPrefetchTiles = 4;             // L2 prefetch distance (query tiles)
   static constexpr int kSBytes = 128 * 128 * 2;       // dS^T tile, bf16
-  static constexpr int kSliceBytes = 128 * 32 * 4;     // one fp32 dQ slice (128 x 32)
-  static constexpr int kReadoutWGs = D / 32;           // warpgroups that reduce dQ
-  static constexpr int kQStagingWGs = kReadoutWGs > 2 ? kReadoutWGs - 2 : 0;  // stage in Q_i
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
@@ -70,6 +69,7 @@ struct BwdCfg {
 struct BwdParams {
   const float* lse;
   const float* Dvec;
+  float* dq_acc;  // fp32 [BH, N, d]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* kv_len;
@@ -108,16 +108,15 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                       const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+                       const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, dq_full, dk_done, dq_free,
-      stats_ready, stage_free, drain;
+      stats_ready, drain;
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
-  __shared__ uint64_t staged[4];  // a warpgroup's dQ slice is in shared memory
   __shared__ __align__(16) float s_nl2[128];  // -lse2 of the tile's query rows
   __shared__ __align__(16) float s_nD[128];   // -D
   __shared__ uint32_t tmem_slot;
@@ -138,23 +137,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&kv_full, 1);
     mbar_init(&s_ready, 1);
     mbar_init(&dp_ready, 1);
-    mbar_init(&p_ready, C::kMathThreads);
-    mbar_init(&ds_ready, C::kMathThreads);
+    mbar_init(&p_ready, C::kMathWarps);  // one arrival per math warp
+    mbar_init(&ds_ready, C::kMathWarps);
     mbar_init(&dq_full, 1);
     mbar_init(&dk_done, 1);
-    mbar_init(&dq_free, C::kMathThreads);
-    mbar_init(&stats_ready, 128);
-    mbar_init(&stage_free, C::kReadoutWGs);
+    mbar_init(&dq_free, C::kMathWarps);
+    mbar_init(&stats_ready, 4);
     mbar_init(&drain, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1 + C::kQStagingWGs);  // MMA commit + staging reads done
+      mbar_init(&q_empty[s], 1);  // dK, the last reader of Q_i, is done
     }
     for (int s = 0; s < C::kDOStages; ++s) {
       mbar_init(&do_full[s], 1);
       mbar_init(&do_empty[s], 1);
     }
-    for (int w = 0; w < 4; ++w) mbar_init(&staged[w], 128);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -171,16 +168,27 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmDO);
-      prefetch_tensormap(&tmDQ);
       mbar_expect_tx(&kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
         tma_load_3d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, bh);
         tma_load_3d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, bh);
       }
       int qcount[C::kQStages] = {}, dcount[C::kDOStages] = {};
+      // L2 prefetch of the Q / dO tiles a few query tiles ahead of their loads,
+      // which then find them in L2 instead of paying the DRAM latency
+      int ipf = qtiles.first(), npf = 0;
+      auto prefetch_upto = [&](int count) {
+        for (; npf < count && ipf < iend; ++npf, ipf = qtiles.next(ipf + 1))
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_prefetch_3d(&tmQ, c * 64, ipf * 128, bh);
+            tma_prefetch_3d(&tmDO, c * 64, ipf * 128, bh);
+          }
+      };
+      prefetch_upto(C::kPrefetchTiles);
       int it = 0;
       for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
+        prefetch_upto(it + 1 + C::kPrefetchTiles);
         if (!mbar_wait(&q_empty[qs], ((it / C::kQStages) & 1) ^ 1, &abort_flag, p.status, 401))
           break;
         mbar_expect_tx(&q_full[qs], C::kTileBytes);
@@ -207,15 +215,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (lane == 0 && iend > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
-      constexpr uint32_t idesc_dq = idesc_bf16(128, D, true, true);     // dQ
+      constexpr uint32_t idesc_dq = idesc_bf16(128, 128, true, true);   // dQ^T (M = d rows, padded)
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
       const uint32_t sQ0 = smem_addr(smem + C::kOffQ), sDO0 = smem_addr(smem + C::kOffDO);
       const uint32_t sDS = smem_addr(smem + C::kOffDS);
+      // operand descriptors: built once per buffer; an operand's K step adds
+      // its byte offset >> 4 to the start-address field (every buffer lies
+      // below 256 KB, so the 14-bit field never carries)
+      const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dK_mn = sdesc_sw128(sK, C::kChunkBytes, 1024);
+      const uint64_t dDS_mn = sdesc_sw128(sDS, C::kChunkBytes, 1024);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
+        const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dQ_mn = sdesc_sw128(sQ, C::kChunkBytes, 1024);
+        const uint64_t dDO_k = sdesc_sw128(sDO, 16, 1024);
+        const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
         ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
         // P^T / dS^T of the previous tile sit in the S^T columns until dK is done
         if (ok && it > 0) ok = mbar_wait(&dk_done, (it - 1) & 1, &abort_flag, p.status, 503);
@@ -224,9 +241,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tmem + C::kColS, sdesc_sw128(sK + koff, 16, 1024), sdesc_sw128(sQ + koff, 16, 1024),
-                 idesc_s, ks > 0);
+          const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
         }
         mma_commit(&s_ready);
         // dQ of the previous tile sits in the dP^T columns until it is read out
@@ -237,9 +253,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // dP^T = V dO^T
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-          mma_ss(tmem + C::kColDP, sdesc_sw128(sV + koff, 16, 1024),
-                 sdesc_sw128(sDO + koff, 16, 1024), idesc_s, ks > 0);
+          const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+          mma_ss(tmem + C::kColDP, dV_k + koff, dDO_k + koff, idesc_s, ks > 0);
         }
         mma_commit(&dp_ready);
         ok = mbar_wait(&p_ready, it & 1, &abort_flag, p.status, 505);
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
-                 sdesc_sw128(sDO + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
+                 dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
         mma_commit(&do_empty[ds]);
         ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
         if (!ok) break;
@@ -260,14 +275,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + C::kColDK, tmem + C::kColS + 32 * (ks >> 1) + 16 + 8 * (ks & 1),
-                 sdesc_sw128(sQ + ks * 2048, C::kChunkBytes, 1024), idesc_acc, acc | (ks > 0));
+                 dQ_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
         mma_commit(&dk_done);
         mma_commit(&q_empty[qs]);
-        // dQ_i = dS K_j into the (consumed) dP^T columns
+        // dQ_i^T = K_j^T dS^T into the (consumed) dP^T columns
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(sDS + ks * 2048, C::kChunkBytes, 1024),
-                 sdesc_sw128(sK + ks * 2048, C::kChunkBytes, 1024), idesc_dq, ks > 0);
+          mma_ss(tmem + C::kColDQ, dK_mn + ks * (2048 >> 4), dDS_mn + ks * (2048 >> 4), idesc_dq,
+                 ks > 0);
         mma_commit(&dq_full);
       }
       mma_commit(&drain);
@@ -280,38 +295,42 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kt * 128 + tq;
     const bool key_live = key < kv_limit;
-    const bool reducer = wg < C::kReadoutWGs;
-    const bool elected = reducer && tq == 0;
     const uint32_t sDS = smem_addr(smem + C::kOffDS);
     const size_t head_row0 = (size_t)bh * p.N;
     const int col0 = wg * 32;               // this warpgroup's query columns
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 sc2 = make_float2(p.scale, p.scale);
-    int it = 0, prev_qs = 0;
+    int it = 0;
     bool ok = true;
-    // Statistics of a query tile, negated, as a thread of the first warpgroup
-    // holds them between the global load and the shared-memory store.
+    // Statistics of one query row: loaded raw (lse, D) by a thread of the
+    // first warpgroup, converted to what the math uses (-lse2, -D) only when
+    // stored, so that the load's latency is not waited for before then.
     struct RowStats {
       float nl2, nd;
     };
     auto load_stats = [&](int qt) {
-      RowStats st{-INFINITY, 0.f};
+      RowStats st{-INFINITY, 0.f};  // rows past the end: P = 0
       const int q = qt * 128 + tid;
       if (qt < iend && q < p.N) {
-        const float l = p.lse[head_row0 + q];
-        if (l != -INFINITY) st.nl2 = -l * kLog2e;  // rows with no visible key: P = 0
-        st.nd = -p.Dvec[head_row0 + q];
+        st.nl2 = p.lse[head_row0 + q];
+        st.nd = p.Dvec[head_row0 + q];
       }
       return st;
     };
+    auto finish_stats = [](RowStats st) {
+      asm volatile("" : "+f"(st.nl2), "+f"(st.nd));  // first use of the loaded values
+      // rows with no visible key (lse = -inf) keep -lse2 = -inf: P = 0
+      st.nl2 = st.nl2 == -INFINITY ? -INFINITY : -st.nl2 * kLog2e;
+      st.nd = -st.nd;
+      return st;
+    };
     if (tid < 128 && iend > 0) {
-      const RowStats st = load_stats(qtiles.first());
+      const RowStats st = finish_stats(load_stats(qtiles.first()));
       s_nl2[tid] = st.nl2;
       s_nD[tid] = st.nd;
-      mbar_arrive(&stats_ready);
+      mbar_arrive_warp(&stats_ready);
     }
     for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-      const int qs = it % C::kQStages;
       // ---- the next tile's statistics: loaded now, stored once every math
       // thread is past this tile's dS (the loads' latency hides behind the MMAs)
       RowStats next_st{};
@@ -355,14 +374,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_ready);
-      // ---- the previous tile's reduce-adds have read their staging memory (the
-      // dS^T tile and Q buffer written below): awaited only now, after P^T
-      if (elected && it > 0) {
-        bulk_wait_read();
-        mbar_arrive(&stage_free);
-        if (wg >= 2) mbar_arrive(&q_empty[prev_qs]);
-      }
+      mbar_arrive_warp(&p_ready);
       // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): bf16 into the
       // swizzled shared-memory tile and packed over S^T columns [col0 + 16, col0 + 32)
       ok = mbar_wait_warp(&dp_ready, it & 1, &abort_flag, p.status, 608);
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
       FA_TMEM_ST16(tmem + C::kColS + lane_off + col0 + 16, dsp);
-      if (it > 0 && !mbar_wait_warp(&stage_free, (it - 1) & 1, &abort_flag, p.status, 605)) break;
+      // (the dS^T tile's last reader, the previous dQ^T MMA, is done: dq_full)
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
         const int c = col0 + 8 * g;
@@ -398,54 +410,40 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&ds_ready);
+      mbar_arrive_warp(&ds_ready);
       // ---- the next tile's statistics replace this tile's once every math
       // thread is past its last read of them (ds_ready complete)
       if (tid < 128) {
-        if (mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 600)) {
-          s_nl2[tid] = next_st.nl2;
-          s_nD[tid] = next_st.nd;
-          mbar_arrive(&stats_ready);
-        } else {
-          ok = false;
-        }
+        if (!mbar_wait_warp(&ds_ready, it & 1, &abort_flag, p.status, 600)) break;
+        const RowStats st = finish_stats(next_st);
+        s_nl2[tid] = st.nl2;
+        s_nD[tid] = st.nd;
+        mbar_arrive_warp(&stats_ready);
       }
-      if (!__all_sync(0xffffffffu, ok)) break;
-      // ---- dQ_i: lanes are query rows
+      // ---- dQ_i^T: lanes are d columns, TMEM columns query rows
       ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
       if (!ok) break;
       tc_fence_after();
       uint32_t r[32];
-      if (reducer) FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
+      FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
       tc_fence_before();
-      mbar_arrive(&dq_free);  // the dP^T / dQ columns may be overwritten now
-      if (reducer) {
-        // staging: slices 0, 1 in the dS^T tile (dQ, its last reader, is done),
-        // 2, 3 in the finished Q_i buffer (dK, its last reader, is done)
-        ok = mbar_wait_warp(&dk_done, it & 1, &abort_flag, p.status, 604);
-        if (!ok) break;
-        uint8_t* stage = wg < 2 ? smem + C::kOffDS + wg * C::kSliceBytes
-                                : smem + C::kOffQ + qs * C::kTileBytes + (wg - 2) * C::kSliceBytes;
-        const uint32_t row_base = smem_addr(stage) + (tq >> 3) * 1024 + (tq & 7) * 128;
+      mbar_arrive_warp(&dq_free);  // the dP^T / dQ^T columns may be overwritten now
+      {
+        const int dcol = tq;                    // this lane's d column
+        const int qrow0 = q0 + col0;            // first of the warpgroup's 32 query rows
+        const int nrows = min(32, p.N - qrow0);  // rows past N are not written
+        if (dcol < D) {
+          float* dst = p.dq_acc + (head_row0 + qrow0) * D + dcol;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)  // 16-byte chunk c of the 128-byte row, XOR-swizzled
-          st_shared_v4(row_base + ((c ^ (tq & 7)) << 4), r[4 * c], r[4 * c + 1], r[4 * c + 2],
-                       r[4 * c + 3]);
-        fence_proxy_async_smem();
-        mbar_arrive(&staged[wg]);
-        if (elected && mbar_wait(&staged[wg], it & 1, &abort_flag, p.status, 606)) {
-          // rows past N fall outside the tensor and are not written
-          tma_reduce_add_3d(&tmDQ, stage, wg * 32, q0, bh);
-          bulk_commit();
+          for (int j = 0; j < 32; ++j)
+            if (j < nrows) red_add_f32(dst + (size_t)j * D, __uint_as_float(r[j]));
         }
       }
-      prev_qs = qs;
     }
-    if (elected) bulk_wait_all();  // this warpgroup's reduce-adds are complete
     // ------------------------------------------------------------ dK, dV out
     // TMEM loads are warp-collective: every lane takes part; only rows inside
-    // the sequence are stored.  dk_done of the last tile (waited above by the
-    // reducing warpgroups) or dq_full (all) cover the last dV / dK MMAs.
+    // the sequence are stored.  dq_full of the last tile, waited above, already
+    // covers its dV / dK MMAs (the tensor core completes them in order).
     if (__all_sync(0xffffffffu, ok && !abort_flag) && it > 0)
       ok = mbar_wait_warp(&dk_done, (it - 1) & 1, &abort_flag, p.status, 607);
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
@@ -484,14 +482,14 @@ template <int D>
 cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
   const int BH = a.B * a.H;
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo;
   if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
-      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128) ||
-      !encode_f32_bhnd_map(&mdq, a.dq_acc, BH, a.N, D))
+      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.D;
+  p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
@@ -507,7 +505,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, mdq, p);
+  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 
