@@ -138,11 +138,9 @@ def run_gpu(args, rank, world, local_rank):
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     rows = B * H * N
     D = ws[: rows * 4].view(torch.float32)
-    off = (rows * 4 + 255) // 256 * 256
-    dq_acc = ws[off: off + rows * d * 4].view(torch.float32)
     stream = torch.cuda.current_stream(dev)
 
-    kernels = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq_convert"]
+    kernels = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
     ev = {n: [] for n in kernels}
 
     def step(record):
@@ -156,10 +154,11 @@ def run_gpu(args, rank, world, local_rank):
             else:
                 fn()
         mark("fwd", lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, stream))
-        mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, dq_acc, B, H, N, d, stream))
-        mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv(q, k, v, do, lse, D, dq_acc, dk, dv, B, H, N, d,
-                                                scale, w.causal, mask, stream))
-        mark("bwd_dq_convert", lambda: fa.fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, stream))
+        mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
+        mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv(q, k, v, do, lse, D, dk, dv, B, H, N, d, scale,
+                                                w.causal, mask, stream))
+        mark("bwd_dq", lambda: fa.fa_bwd_dq(q, k, v, do, lse, D, dq, B, H, N, d, scale, w.causal,
+                                            mask, stream))
 
     dist = None
     if world > 1:
@@ -210,8 +209,13 @@ def run_gpu(args, rank, world, local_rank):
         return None
     peaks, peak_kind = measured_peaks()
     peak = peaks["bf16_tflops"]
-    dkdv_flops = 2.5 * fwd_flops
+    # per kernel, the GEMM work it does (each GEMM of the backward = fwd_flops / 2):
+    # dK/dV kernel S^T, dP^T, dV, dK (all of them part of the 2.5x algorithmic
+    # count); dQ kernel S, dP, dQ (only dQ algorithmic, S and dP recomputed again)
+    dkdv_flops = 2.0 * fwd_flops
+    dq_flops = 1.5 * fwd_flops
     achieved = dkdv_flops / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
+    dq_achieved = dq_flops / (per_kernel["bwd_dq"] * 1e-3) / 1e12
     fwd_achieved = fwd_flops / (per_kernel["fwd"] * 1e-3) / 1e12
     result = {
         "metric": METRIC,
@@ -236,7 +240,7 @@ def run_gpu(args, rank, world, local_rank):
         "pct_of_peak": round(100.0 * (value / world) / peak, 2),
         "kernels_ms": {n: round(t, 4) for n, t in per_kernel.items()},
         "roofline": {
-            "kernel": "fa_bwd_dkdv (S, dP, dV, dK, dQ on tcgen05)",
+            "kernel": "fa_bwd_dkdv (S^T, dP^T, dV, dK on tcgen05)",
             "bound": "tensor",
             "achieved": round(achieved, 2),
             "peak": peak,
@@ -248,6 +252,9 @@ def run_gpu(args, rank, world, local_rank):
         },
         "fwd_roofline": {"kernel": "fa_fwd", "achieved": round(fwd_achieved, 2),
                          "frac": round(fwd_achieved / peak, 4), "flops_per_launch": fwd_flops},
+        "dq_roofline": {"kernel": "fa_bwd_dq (S, dP, dQ on tcgen05; S and dP recomputed)",
+                        "achieved": round(dq_achieved, 2), "frac": round(dq_achieved / peak, 4),
+                        "flops_per_launch": dq_flops},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }

@@ -14,7 +14,7 @@ import os
 
 __all__ = [
     "FaError", "FaMask", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
-    "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq_convert", "fa_fwd_fp32", "fa_bwd_fp32",
+    "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_fwd_fp32", "fa_bwd_fp32",
     "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
     "make_mask", "forward", "backward", "LIB_PATH",
     "FA_MASK_NONE", "FA_MASK_KEY_PADDING", "FA_MASK_BLOCK_SPARSE", "STATUS",
@@ -58,9 +58,9 @@ _SIGS = {
     "fa_bwd_workspace_size": [_i, _i, _i, _i],
     "fa_bwd": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_bwd_fp32": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _p],
-    "fa_bwd_preprocess": [_p, _p, _p, _p, _i, _i, _i, _i, _p],
-    "fa_bwd_dkdv": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
-    "fa_bwd_dq_convert": [_p, _p, _i, _i, _i, _i, _p],
+    "fa_bwd_preprocess": [_p, _p, _p, _i, _i, _i, _i, _p],
+    "fa_bwd_dkdv": [_p] * 8 + [_i, _i, _i, _i, _f, _i, _mp, _p],
+    "fa_bwd_dq": [_p] * 7 + [_i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_status_string": [_i],
     "fa_get_device_status": [_p, ctypes.POINTER(ctypes.c_int)],
     "fa_debug_umma_gemm": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p],
@@ -139,21 +139,20 @@ def fa_bwd_fp32(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, 
                            scale, int(causal), mask, _stream(stream)), "fa_bwd_fp32")
 
 
-def fa_bwd_preprocess(o, dO, D, dq_acc, B, H, N, d, stream=None):
-    _check(lib.fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), _ptr(dq_acc), B, H, N, d,
-                                 _stream(stream)), "fa_bwd_preprocess")
+def fa_bwd_preprocess(o, dO, D, B, H, N, d, stream=None):
+    _check(lib.fa_bwd_preprocess(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d, _stream(stream)),
+           "fa_bwd_preprocess")
 
 
-def fa_bwd_dkdv(q, k, v, dO, lse, D, dq_acc, dk, dv, B, H, N, d, scale, causal, mask=None,
-                stream=None):
-    _check(lib.fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D),
-                           _ptr(dq_acc), _ptr(dk), _ptr(dv), B, H, N, d, scale, int(causal),
-                           mask, _stream(stream)), "fa_bwd_dkdv")
+def fa_bwd_dkdv(q, k, v, dO, lse, D, dk, dv, B, H, N, d, scale, causal, mask=None, stream=None):
+    _check(lib.fa_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dk),
+                           _ptr(dv), B, H, N, d, scale, int(causal), mask, _stream(stream)),
+           "fa_bwd_dkdv")
 
 
-def fa_bwd_dq_convert(dq_acc, dq, B, H, N, d, stream=None):
-    _check(lib.fa_bwd_dq_convert(_ptr(dq_acc), _ptr(dq), B, H, N, d, _stream(stream)),
-           "fa_bwd_dq_convert")
+def fa_bwd_dq(q, k, v, dO, lse, D, dq, B, H, N, d, scale, causal, mask=None, stream=None):
+    _check(lib.fa_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq),
+                         B, H, N, d, scale, int(causal), mask, _stream(stream)), "fa_bwd_dq")
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20   # FA_NOALLOC_SCRATCH_BYTES

@@ -22,6 +22,7 @@ SOURCES = [
     "fa_api.cu",
     "fa_fwd_sm103.cu",
     "fa_bwd_sm103.cu",
+    "fa_bwd_dq_sm103.cu",
     "fa_bwd_aux.cu",
     "fa_fp32.cu",
     "fa_probe.cu",

@@ -87,19 +87,6 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, i
   return r == CUDA_SUCCESS;
 }
 
-bool encode_f32_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
-  cuuint32_t box[3] = {32, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 int* device_status() {
   static int* ptrs[kMaxDevices] = {nullptr};
   static std::mutex mu;
@@ -162,12 +149,8 @@ static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float s
 static fa_status split_workspace(BwdArgs* a, void* ws, size_t ws_bytes) {
   if (!ws) return FA_ERR_WORKSPACE;
   if (!aligned16(ws)) return FA_ERR_ALIGNMENT;
-  if (ws_bytes < round256((size_t)a->B * a->H * a->N * sizeof(float)) +
-                     round256((size_t)a->B * a->H * a->N * a->d * sizeof(float)))
-    return FA_ERR_WORKSPACE;
-  const size_t rows = (size_t)a->B * a->H * a->N;
+  if (ws_bytes < round256((size_t)a->B * a->H * a->N * sizeof(float))) return FA_ERR_WORKSPACE;
   a->D = static_cast<float*>(ws);
-  a->dq_acc = reinterpret_cast<float*>(static_cast<char*>(ws) + round256(rows * sizeof(float)));
   return FA_OK;
 }
 
@@ -197,8 +180,7 @@ const char* fa_status_string(fa_status s) {
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d) != FA_OK) return 0;
-  const size_t rows = (size_t)B * H * N;
-  return round256(rows * sizeof(float)) + round256(rows * d * sizeof(float));
+  return round256((size_t)B * H * N * sizeof(float));
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -239,50 +221,52 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   fa_status st2 = launched(launch_bwd_preprocess(a, s));
   if (st2 == FA_OK) st2 = launched(launch_bwd_dkdv_bf16(a, s));
-  if (st2 == FA_OK) st2 = launched(launch_bwd_dq_convert(a, s));
+  if (st2 == FA_OK) st2 = launched(launch_bwd_dq_bf16(a, s));
   return st2;
 }
 
-fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H,
-                            int N, int d, void* stream) {
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                            void* stream) {
   BwdArgs a{};
   fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr);
   if (st != FA_OK) return st;
-  if (!o || !dO || !D || !dq_acc) return FA_ERR_INVALID_ARG;
-  if (!aligned16(o) || !aligned16(dO) || !aligned4(D) || !aligned16(dq_acc))
-    return FA_ERR_ALIGNMENT;
-  a.o = o; a.dO = dO; a.D = D; a.dq_acc = dq_acc;
+  if (!o || !dO || !D) return FA_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(dO) || !aligned4(D)) return FA_ERR_ALIGNMENT;
+  a.o = o; a.dO = dO; a.D = D;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_bwd_preprocess(a, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
-                      const float* lse, const float* D, float* dq_acc, void* dk, void* dv, int B,
-                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
-                      void* stream) {
+                      const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
+                      int d, float scale, int causal, const fa_mask* mask, void* stream) {
   BwdArgs a{};
   fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
   if (st != FA_OK) return st;
-  if (!q || !k || !v || !dO || !lse || !D || !dq_acc || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !dO || !lse || !D || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
-      !aligned4(D) || !aligned16(dq_acc) || !aligned16(dk) || !aligned16(dv))
+      !aligned4(D) || !aligned16(dk) || !aligned16(dv))
     return FA_ERR_ALIGNMENT;
   a.q = q; a.k = k; a.v = v; a.dO = dO; a.lse = lse;
-  a.D = const_cast<float*>(D); a.dq_acc = dq_acc; a.dk = dk; a.dv = dv;
+  a.D = const_cast<float*>(D); a.dk = dk; a.dv = dv;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_bwd_dkdv_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
-fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
-                            void* stream) {
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                    const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                    const fa_mask* mask, void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr);
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
   if (st != FA_OK) return st;
-  if (!dq_acc || !dq) return FA_ERR_INVALID_ARG;
-  if (!aligned16(dq_acc) || !aligned16(dq)) return FA_ERR_ALIGNMENT;
-  a.dq_acc = const_cast<float*>(dq_acc); a.dq = dq;
+  if (!q || !k || !v || !dO || !lse || !D || !dq) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
+      !aligned4(D) || !aligned16(dq))
+    return FA_ERR_ALIGNMENT;
+  a.q = q; a.k = k; a.v = v; a.dO = dO; a.lse = lse;
+  a.D = const_cast<float*>(D); a.dq = dq;
   if (!attach_status(&a)) return FA_ERR_CUDA;
-  return launched(launch_bwd_dq_convert(a, static_cast<cudaStream_t>(stream)));
+  return launched(launch_bwd_dq_bf16(a, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const float* o,

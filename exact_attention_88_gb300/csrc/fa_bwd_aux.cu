@@ -1,8 +1,7 @@
-// Memory-bound steps around the backward kernel:
-//   preprocess : D_i = sum_c dO_ic * O_ic (fp32) and dq_acc = 0
-//   dq convert : dq = bf16(dq_acc), round to nearest even
-// Both stream their operands once with 16-byte accesses; grids are a multiple
-// of the SM count and loop over the data.
+// Memory-bound step ahead of the backward kernels:
+//   preprocess : D_i = sum_c dO_ic * O_ic (fp32)
+// It streams O and dO once with 16-byte accesses; the grid is a multiple of
+// the SM count and loops over the rows.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -24,8 +23,7 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __restrict__ o,
                                                              const uint4* __restrict__ dO,
                                                              float* __restrict__ Dout,
-                                                             float4* __restrict__ dq_acc,
-                                                             long long rows, long long acc4) {
+                                                             long long rows) {
   constexpr int G = D / 8;  // lanes per row (8 or 16)
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
@@ -54,47 +52,20 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint4* __rest
     for (int off = G / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (row < rows && g == 0) Dout[row] = acc;
   }
-  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (long long i = tid; i < acc4; i += nthreads) dq_acc[i] = z;
-}
-
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc,
-                                                         uint4* __restrict__ out, long long n8) {
-  const long long nthreads = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += nthreads) {
-    const float4 a = acc[2 * i], b = acc[2 * i + 1];
-    uint4 w;
-    w.x = pack_bf16(a.x, a.y);
-    w.y = pack_bf16(a.z, a.w);
-    w.z = pack_bf16(b.x, b.y);
-    w.w = pack_bf16(b.z, b.w);
-    out[i] = w;
-  }
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const long long rows = (long long)a.B * a.H * a.N;
-  const long long acc4 = rows * a.d / 4;
   const int threads = 256;
   const int grid = grid_for(rows * (a.d / 8), threads);
   if (a.d == 64)
     bwd_preprocess_kernel<64><<<grid, threads, 0, s>>>(
-        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D,
-        reinterpret_cast<float4*>(a.dq_acc), rows, acc4);
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D, rows);
   else
     bwd_preprocess_kernel<128><<<grid, threads, 0, s>>>(
-        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D,
-        reinterpret_cast<float4*>(a.dq_acc), rows, acc4);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t s) {
-  const long long n8 = (long long)a.B * a.H * a.N * a.d / 8;
-  const int threads = 256;
-  dq_convert_kernel<<<grid_for(n8, threads), threads, 0, s>>>(
-      reinterpret_cast<const float4*>(a.dq_acc), static_cast<uint4*>(a.dq), n8);
+        static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dO), a.D, rows);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,394 @@
+// Backward pass of exact attention, dQ, on sm_103a tensor cores: one CTA owns
+// a 128-row query tile Q_i of one (batch, head), walks the key tiles K_j, V_j
+// it can see, recomputes P from Q, K and the saved lse ("FlashAttention: Fast
+// and Memory-Efficient Exact Attention with IO-Awareness", summary page, "Key
+// ideas: recomputation in the backward pass") and accumulates
+//   dQ_i = scale sum_j dS_ij K_j,  dS = P o (dP - D),  dP = dO V^T
+// in TMEM.  Each dQ row is owned by one CTA, so it needs no atomics and the
+// result does not depend on scheduling.  (The gradient formulas are the
+// textbook derivative of the definition; the pages do not print them.)
+//
+// Query rows sit on the TMEM lanes, so lse and D are one scalar per thread.
+// TMEM columns: S_0 [0,128) and S_1 [128,256) (S_j alternates between them;
+// after the math has read S_j, packed bf16 dS_j goes over its first half),
+// dP [256,384), dQ accumulator [384, 384+d).
+// Tensor-core order per key tile u (prologue: S_0, dP_0, S_1):
+//   dQ += dS_u K_u   A = dS_u from TMEM, B = K_u (MN-major)
+//   dP_{u+1} = dO V_{u+1}^T
+//   S_{u+2} = Q K_{u+2}^T   into the buffer dS_u occupied (after dQ_u is done)
+// so that while the math warps compute P_{u+1} and dS_{u+1}, the tensor core
+// has dQ_u, dP_{u+1} and S_{u+2} queued.
+//
+// Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// key columns [32w, 32w+32) of S / dP and d columns [w d/4, (w+1) d/4) of the
+// dQ read-out; warp 16 is the TMA producer; warp 17 issues the MMAs.
+#include "fa_common.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kKStages = 3;        // K_j lives from S_j to dQ_j: one tile longer than V_j
+  static constexpr int kVStages = 2;
+  static constexpr int kPrefetchTiles = 4;  // L2 prefetch distance (key tiles)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTileBytes;
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr int kSmem = kOffV + kVStages * kTileBytes + 1024;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
+  static constexpr int kMathWarps = 16;
+  static constexpr int kThreads = kMathWarps * 32 + 64;
+  static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-out
+};
+
+struct DqParams {
+  const float* lse;
+  const float* Dvec;
+  __nv_bfloat16* dq;
+  const int32_t* kv_len;
+  const uint8_t* block_mask;
+  int H, N, T, BH;
+  float scale, scale_log2;
+  int causal;
+  int* status;
+};
+
+// Key tiles j that query tile qi sees: j < jend (causal diagonal, key
+// padding, end of sequence), block-mask row qi.
+struct KTileIter {
+  const uint8_t* row;  // block-mask row or nullptr
+  int jend;
+  __device__ int next(int j) const {
+    if (row)
+      while (j < jend && row[j] == 0) ++j;
+    return j;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const DqParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t q_full, dp_full, ds_ready, dq_done, drain;
+  __shared__ uint64_t s_full[2];
+  __shared__ uint64_t k_full[C::kKStages], k_empty[C::kKStages];
+  __shared__ uint64_t v_full[C::kVStages], v_empty[C::kVStages];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lin = blockIdx.x;
+  const int qi = p.T - 1 - lin / p.BH;  // causal: the last query tiles see the most keys: first
+  const int bh = lin % p.BH;
+  const int b = bh / p.H;
+  int kv_limit = p.N;
+  if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
+  const int jkv = (kv_limit + 127) / 128;
+  const KTileIter ktiles{p.block_mask ? p.block_mask + (size_t)qi * p.T : nullptr,
+                         p.causal ? min(jkv, qi + 1) : jkv};
+  const int jfirst = ktiles.next(0);
+  const bool any = jfirst < ktiles.jend;
+
+  if (tid == 0) {
+    mbar_init(&q_full, 1);
+    mbar_init(&dp_full, 1);
+    mbar_init(&ds_ready, C::kMathWarps);  // one arrival per math warp
+    mbar_init(&dq_done, 1);
+    mbar_init(&drain, 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
+    for (int s = 0; s < C::kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < C::kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == C::kMathWarps + 1) tmem_alloc(&tmem_slot, C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == C::kMathWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && any) {
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmDO);
+      mbar_expect_tx(&q_full, 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qi * 128, bh);
+        tma_load_3d(&tmDO, &q_full, smem + C::kOffDO + c * C::kChunkBytes, c * 64, qi * 128, bh);
+      }
+      int jpf = jfirst, npf = 0;
+      auto prefetch_upto = [&](int count) {
+        for (; npf < count && jpf < ktiles.jend; ++npf, jpf = ktiles.next(jpf + 1))
+          for (int c = 0; c < C::kChunks; ++c) {
+            tma_prefetch_3d(&tmK, c * 64, jpf * 128, bh);
+            tma_prefetch_3d(&tmV, c * 64, jpf * 128, bh);
+          }
+      };
+      prefetch_upto(C::kPrefetchTiles);
+      int kcount[C::kKStages] = {}, vcount[C::kVStages] = {};
+      int u = 0;
+      for (int j = jfirst; j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+        prefetch_upto(u + 1 + C::kPrefetchTiles);
+        const int ks = u % C::kKStages, vs = u % C::kVStages;
+        if (!mbar_wait(&k_empty[ks], ((u / C::kKStages) & 1) ^ 1, &abort_flag, p.status, 701))
+          break;
+        mbar_expect_tx(&k_full[ks], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmK, &k_full[ks], smem + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, bh);
+        ++kcount[ks];
+        if (!mbar_wait(&v_empty[vs], ((u / C::kVStages) & 1) ^ 1, &abort_flag, p.status, 702))
+          break;
+        mbar_expect_tx(&v_full[vs], C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(&tmV, &v_full[vs], smem + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, bh);
+        ++vcount[vs];
+      }
+      // every issued copy must have landed before the CTA may exit
+      mbar_drain(&q_full, 0);
+      for (int s = 0; s < C::kKStages; ++s)
+        if (kcount[s]) mbar_drain(&k_full[s], (kcount[s] - 1) & 1);
+      for (int s = 0; s < C::kVStages; ++s)
+        if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
+    }
+  } else if (warp == C::kMathWarps + 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && any) {
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);  // S, dP
+      constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);    // dQ (A in TMEM)
+      // operand descriptors built once; a K step adds its byte offset >> 4
+      // to the start-address field (all buffers lie below 256 KB: no carry)
+      const uint64_t dQ_k = sdesc_sw128(smem_addr(smem + C::kOffQ), 16, 1024);
+      const uint64_t dDO_k = sdesc_sw128(smem_addr(smem + C::kOffDO), 16, 1024);
+      const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
+      // S_u = Q K_u^T into buffer x; dP_u = dO V_u^T
+      auto issue_s = [&](int u, int x) -> bool {
+        const int ks = u % C::kKStages;
+        if (!mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 801)) return false;
+        tc_fence_after();
+        const uint64_t dK_k = sdesc_sw128(sK + ks * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kColS + 128 * x, dQ_k + off, dK_k + off, idesc_s, kk > 0);
+        }
+        mma_commit(&s_full[x]);
+        return true;
+      };
+      auto issue_dp = [&](int u) -> bool {
+        const int vs = u % C::kVStages;
+        if (!mbar_wait(&v_full[vs], (u / C::kVStages) & 1, &abort_flag, p.status, 802)) return false;
+        tc_fence_after();
+        const uint64_t dV_k = sdesc_sw128(sV + vs * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kColDP, dDO_k + off, dV_k + off, idesc_s, kk > 0);
+        }
+        mma_commit(&dp_full);
+        mma_commit(&v_empty[vs]);
+        return true;
+      };
+      bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 800);
+      const int j1 = ktiles.next(jfirst + 1);
+      if (ok) ok = issue_s(0, 0);
+      if (ok) ok = issue_dp(0);
+      if (ok && j1 < ktiles.jend) ok = issue_s(1, 1);
+      int u = 0;
+      for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+        const int x = u & 1;
+        ok = mbar_wait(&ds_ready, u & 1, &abort_flag, p.status, 803);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS_u K_u: dS_u packed in the first half of buffer x (warpgroup
+        // w's keys [32w, 32w+32) in columns [32w, 32w+16)); K_u read MN-major
+        const uint64_t dK_mn = sdesc_sw128(sK + (u % C::kKStages) * C::kTileBytes, C::kChunkBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * x + 32 * (kk >> 1) + 8 * (kk & 1),
+                 dK_mn + kk * (2048 >> 4), idesc_dq, (u > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&dq_done);
+        mma_commit(&k_empty[u % C::kKStages]);
+        const int jn = ktiles.next(j + 1);
+        if (jn < ktiles.jend) {
+          ok = issue_dp(u + 1);  // the math has read dP_u (ds_ready)
+          if (!ok) break;
+          if (ktiles.next(jn + 1) < ktiles.jend) {
+            // buffer x is free once dQ_u, the last reader of dS_u, is done
+            ok = mbar_wait(&dq_done, u & 1, &abort_flag, p.status, 804);
+            if (ok) ok = issue_s(u + 2, x);
+          }
+        }
+      }
+      mma_commit(&drain);
+      mbar_drain(&drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ math warpgroups
+    const int wg = warp >> 2;
+    const int tq = tid & 127;  // TMEM lane: query row of the tile
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int q = qi * 128 + tq;
+    const int col0 = wg * 32;  // this warpgroup's key columns
+    float nl2 = -INFINITY, nd = 0.f;  // -lse2 (rows with no visible key: P = 0), -D
+    if (q < p.N) {
+      const float l = p.lse[(size_t)bh * p.N + q];
+      if (l != -INFINITY) nl2 = -l * kLog2e;
+      nd = -p.Dvec[(size_t)bh * p.N + q];
+    }
+    const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nl22 = make_float2(nl2, nl2);
+    const float2 sc2 = make_float2(p.scale, p.scale), nd2 = make_float2(nd, nd);
+    int u = 0;
+    bool ok = true;
+    for (int j = jfirst; j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+      const int x = u & 1;
+      const uint32_t tS = tmem + C::kColS + 128 * x + lane_off + col0;
+      ok = mbar_wait_warp(&s_full[x], (u >> 1) & 1, &abort_flag, p.status, 901);
+      if (!ok) break;
+      tc_fence_after();
+      // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
+      // causal, key <= q
+      const int key0 = j * 128 + col0;
+      int lim = kv_limit - key0;
+      if (p.causal) lim = min(lim, q - key0 + 1);
+      const bool partial = lim < 32;
+      float pf[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t rs[16];
+        FA_TMEM_LD16_SYNC(tS + 16 * h, rs);
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float2 t = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl22);
+          pf[16 * h + e] = ex2(t.x);
+          pf[16 * h + e + 1] = ex2(t.y);
+        }
+      }
+      if (partial) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (e >= lim) pf[e] = 0.f;
+      }
+      ok = mbar_wait_warp(&dp_full, u & 1, &abort_flag, p.status, 902);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dsp[16];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t rp[16];
+        FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + col0 + 16 * h, rp);
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])), nd2);
+          const float2 dsv = mul2(mul2(make_float2(pf[16 * h + e], pf[16 * h + e + 1]), sc2), t);
+          dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
+        }
+      }
+      // packed dS of keys [col0, col0 + 32) over S columns [col0, col0 + 16),
+      // which this thread has read
+      FA_TMEM_ST16(tS, dsp);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(&ds_ready);
+    }
+    // ------------------------------------------------------------ epilogue
+    bool have = false;
+    if (__all_sync(0xffffffffu, ok && !abort_flag) && u > 0)
+      have = mbar_wait_warp(&dq_done, (u - 1) & 1, &abort_flag, p.status, 903);
+    if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
+      tc_fence_after();
+      uint32_t r[C::kDSlice];
+      if (have) {
+        if constexpr (C::kDSlice == 32) {
+          FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
+        } else {
+          FA_TMEM_LD16_SYNC(tmem + C::kColDQ + lane_off + wg * C::kDSlice, r);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < C::kDSlice; ++e) r[e] = 0u;  // no visible key: dQ = 0
+      }
+      if (q < p.N) {
+        uint4* dst = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * p.N + q) * D + wg * C::kDSlice);
+#pragma unroll
+        for (int g = 0; g < C::kDSlice / 8; ++g) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
+          w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
+          w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
+          w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
+          dst[g] = w;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::kMathWarps + 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
+  using C = DqCfg<D>;
+  const int BH = a.B * a.H;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
+      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128))
+    return cudaErrorInvalidValue;
+  DqParams p;
+  p.lse = a.lse;
+  p.Dvec = a.D;
+  p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
+  p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
+  p.H = a.H;
+  p.N = a.N;
+  p.T = tiles_of(a.N, 128);
+  p.BH = BH;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * kLog2e;
+  p.causal = a.causal;
+  p.status = a.status;
+  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  fa_bwd_dq_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch_dq_d<64>(a, s) : launch_dq_d<128>(a, s);
+}
+
+}  // namespace fa

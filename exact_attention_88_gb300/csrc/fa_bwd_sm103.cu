@@ -1,39 +1,32 @@
-// Backward pass of exact attention on sm_103a tensor cores: dK, dV and the
-// dQ contributions, with P recomputed on chip from Q, K and lse ("FlashAttention:
-// Fast and Memory-Efficient Exact Attention with IO-Awareness", summary page,
-// "Key ideas: recomputation in the backward pass").  The gradient formulas
-// are the textbook derivative of the definition (the pages do not print
-// them): with S = scale Q K^T, P = exp(S - lse), D_i = rowsum(dO o O)_i,
-//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
-//   dK = scale dS^T Q,  dQ = scale dS K.
+// Backward pass of exact attention on sm_103a tensor cores, dK and dV, with P
+// recomputed on chip from Q, K and lse ("FlashAttention: Fast and
+// Memory-Efficient Exact Attention with IO-Awareness", summary page, "Key
+// ideas: recomputation in the backward pass").  The gradient formulas are the
+// textbook derivative of the definition (the pages do not print them): with
+// S = scale Q K^T, P = exp(S - lse), D_i = rowsum(dO o O)_i,
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dK = scale dS^T Q.
+// dQ = scale dS K has a kernel of its own (one CTA per query tile, no atomics).
 //
 // One CTA owns a 128-key tile K_j, V_j of one (batch, head) and walks the
 // query tiles Q_i that can see it (causal: i >= j; block-sparse: mask[i][j]).
 // Everything is computed transposed, keys on the TMEM lanes.  TMEM columns:
 //   [0, d)          dV accumulator          [d, 2d)        dK accumulator
-//   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T and dS^T (bf16, packed two per
-//                   column: warpgroup w's P^T in [32w, 32w+16), dS^T in
-//                   [32w+16, 32w+32))
-//   [2d+128, +128)  dP^T = V_j dO_i^T, then dQ_i = dS K_j (d columns)
+//   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T (bf16, packed two per column:
+//                   warpgroup w's 32 query columns in [32w, 32w+16))
+//   [2d+128, +128)  dP^T = V_j dO_i^T, then dS^T (packed the same way)
 // Per query tile, in tensor-core order, with the math overlapping:
-//   S^T            both operands K-major in shared memory
-//   dP^T           (meanwhile the math computes P^T = 2^(c S^T - lse2_i) into TMEM)
+//   S^T            both operands K-major in shared memory (after the previous
+//                  dV, the last reader of P^T)
+//   dP^T           (after the previous dK, the last reader of dS^T; meanwhile
+//                  the math computes P^T = 2^(c S^T - lse2_i) into TMEM)
 //   dV += P^T dO_i A from TMEM (meanwhile the math computes
-//                  dS^T = scale P^T o (dP^T - D_i) into TMEM and shared memory)
+//                  dS^T = scale P^T o (dP^T - D_i) into TMEM)
 //   dK += dS^T Q_i A from TMEM
-//   dQ_i^T = K_j^T dS^T   both operands MN-major in shared memory (K_j and the
-//                  dS^T tile); M = 128 rows of d (for d = 64 the upper 64 rows
-//                  read past K_j and are never used)
-// The next tile's S^T waits only for dK (the last reader of the S^T columns).
-// The math warps load dQ_i^T from TMEM (which frees those columns for the
-// next dP^T at once): a warp holds 32 consecutive d columns of 32 query rows,
-// so each fp32 atomic add it issues covers 128 contiguous bytes of one row of
-// the dQ accumulator -- no shared-memory staging, no bulk reduce.
+// so the next tile's S^T queues behind dK without waiting for it.
 //
 // Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
-// query columns [32w, 32w+32) of S^T / dP^T / dQ^T and d columns
-// [w d/4, (w+1) d/4) of dK, dV; warp 16 is the TMA producer; warp 17 issues
-// the MMAs.
+// query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4)
+// of dK, dV; warp 16 is the TMA producer; warp 17 issues the MMAs.
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -47,19 +40,16 @@ struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kChunks = D / 64;
-  static constexpr int kQStages = (D == 64) ? 3 : 2;   // Q ring
-  static constexpr int kDOStages = (D == 64) ? 3 : 2;  // dO ring
+  static constexpr int kQStages = (D == 64) ? 4 : 3;   // Q ring (Q_i lives from S^T to dK)
+  static constexpr int kDOStages = (D == 64) ? 4 : 2;  // dO ring
   static constexpr int kPrefetchTiles = 4;             // L2 prefetch distance (query tiles)
-  static constexpr int kSBytes = 128 * 128 * 2;       // dS^T tile, bf16
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTileBytes;
   static constexpr int kOffQ = 2 * kTileBytes;
   static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;
-  static constexpr int kOffDS = kOffDO + kDOStages * kTileBytes;
-  static constexpr int kSmem = kOffDS + kSBytes + 1024;
+  static constexpr int kSmem = kOffDO + kDOStages * kTileBytes + 1024;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
-  static constexpr uint32_t kColDQ = kColDP;
   static constexpr int kMathWarps = 16;
   static constexpr int kMathThreads = kMathWarps * 32;
   static constexpr int kThreads = kMathThreads + 64;
@@ -69,7 +59,6 @@ struct BwdCfg {
 struct BwdParams {
   const float* lse;
   const float* Dvec;
-  float* dq_acc;  // fp32 [BH, N, d]
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   const int32_t* kv_len;
@@ -113,8 +102,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, dq_full, dk_done, dq_free,
-      stats_ready, drain;
+  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, dv_done, dk_done, stats_ready,
+      drain;
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
   __shared__ __align__(16) float s_nl2[128];  // -lse2 of the tile's query rows
@@ -139,9 +128,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&dp_ready, 1);
     mbar_init(&p_ready, C::kMathWarps);  // one arrival per math warp
     mbar_init(&ds_ready, C::kMathWarps);
-    mbar_init(&dq_full, 1);
+    mbar_init(&dv_done, 1);
     mbar_init(&dk_done, 1);
-    mbar_init(&dq_free, C::kMathWarps);
     mbar_init(&stats_ready, 4);
     mbar_init(&drain, 1);
     for (int s = 0; s < C::kQStages; ++s) {
@@ -215,16 +203,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (lane == 0 && iend > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
-      constexpr uint32_t idesc_dq = idesc_bf16(128, 128, true, true);   // dQ^T (M = d rows, padded)
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
       const uint32_t sQ0 = smem_addr(smem + C::kOffQ), sDO0 = smem_addr(smem + C::kOffDO);
-      const uint32_t sDS = smem_addr(smem + C::kOffDS);
       // operand descriptors: built once per buffer; an operand's K step adds
       // its byte offset >> 4 to the start-address field (every buffer lies
       // below 256 KB, so the 14-bit field never carries)
       const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dK_mn = sdesc_sw128(sK, C::kChunkBytes, 1024);
-      const uint64_t dDS_mn = sdesc_sw128(sDS, C::kChunkBytes, 1024);
       bool ok = mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
@@ -234,8 +218,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint64_t dDO_k = sdesc_sw128(sDO, 16, 1024);
         const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
         ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
-        // P^T / dS^T of the previous tile sit in the S^T columns until dK is done
-        if (ok && it > 0) ok = mbar_wait(&dk_done, (it - 1) & 1, &abort_flag, p.status, 503);
+        // P^T of the previous tile sits in the S^T columns until dV is done
+        if (ok && it > 0) ok = mbar_wait(&dv_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
         tc_fence_after();
         // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
@@ -245,8 +229,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
         }
         mma_commit(&s_ready);
-        // dQ of the previous tile sits in the dP^T columns until it is read out
-        if (it > 0) ok = mbar_wait(&dq_free, (it - 1) & 1, &abort_flag, p.status, 504);
+        // dS^T of the previous tile sits in the dP^T columns until dK is done
+        if (it > 0) ok = mbar_wait(&dk_done, (it - 1) & 1, &abort_flag, p.status, 504);
         if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
         if (!ok) break;
         tc_fence_after();
@@ -267,23 +251,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
                  dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
+        mma_commit(&dv_done);
         mma_commit(&do_empty[ds]);
         ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
         if (!ok) break;
         tc_fence_after();
-        // dK += dS^T Q (dS^T in TMEM, packed in columns [32w+16, 32w+32))
+        // dK += dS^T Q (dS^T in TMEM: warpgroup w's columns packed in [32w, 32w+16)
+        // of the dP^T region)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + C::kColDK, tmem + C::kColS + 32 * (ks >> 1) + 16 + 8 * (ks & 1),
+          mma_ts(tmem + C::kColDK, tmem + C::kColDP + 32 * (ks >> 1) + 8 * (ks & 1),
                  dQ_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
         mma_commit(&dk_done);
         mma_commit(&q_empty[qs]);
-        // dQ_i^T = K_j^T dS^T into the (consumed) dP^T columns
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ss(tmem + C::kColDQ, dK_mn + ks * (2048 >> 4), dDS_mn + ks * (2048 >> 4), idesc_dq,
-                 ks > 0);
-        mma_commit(&dq_full);
       }
       mma_commit(&drain);
       mbar_drain(&drain, 0);
@@ -295,7 +275,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kt * 128 + tq;
     const bool key_live = key < kv_limit;
-    const uint32_t sDS = smem_addr(smem + C::kOffDS);
     const size_t head_row0 = (size_t)bh * p.N;
     const int col0 = wg * 32;               // this warpgroup's query columns
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
@@ -375,8 +354,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&p_ready);
-      // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): bf16 into the
-      // swizzled shared-memory tile and packed over S^T columns [col0 + 16, col0 + 32)
+      // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): packed bf16
+      // over dP^T columns [col0, col0 + 16), which this thread has read
       ok = mbar_wait_warp(&dp_ready, it & 1, &abort_flag, p.status, 608);
       if (!ok) break;
       tc_fence_after();
@@ -399,16 +378,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
       }
-      FA_TMEM_ST16(tmem + C::kColS + lane_off + col0 + 16, dsp);
-      // (the dS^T tile's last reader, the previous dQ^T MMA, is done: dq_full)
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int c = col0 + 8 * g;
-        st_shared_v4(sDS + (c >> 6) * C::kChunkBytes + sw128_offset(tq, c & 63), dsp[4 * g],
-                     dsp[4 * g + 1], dsp[4 * g + 2], dsp[4 * g + 3]);
-      }
+      FA_TMEM_ST16(tmem + C::kColDP + lane_off + col0, dsp);
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive_warp(&ds_ready);
       // ---- the next tile's statistics replace this tile's once every math
@@ -420,30 +391,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         s_nD[tid] = st.nd;
         mbar_arrive_warp(&stats_ready);
       }
-      // ---- dQ_i^T: lanes are d columns, TMEM columns query rows
-      ok = mbar_wait_warp(&dq_full, it & 1, &abort_flag, p.status, 603);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t r[32];
-      FA_TMEM_LD32_SYNC(tmem + C::kColDQ + lane_off + wg * 32, r);
-      tc_fence_before();
-      mbar_arrive_warp(&dq_free);  // the dP^T / dQ^T columns may be overwritten now
-      {
-        const int dcol = tq;                    // this lane's d column
-        const int qrow0 = q0 + col0;            // first of the warpgroup's 32 query rows
-        const int nrows = min(32, p.N - qrow0);  // rows past N are not written
-        if (dcol < D) {
-          float* dst = p.dq_acc + (head_row0 + qrow0) * D + dcol;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nrows) red_add_f32(dst + (size_t)j * D, __uint_as_float(r[j]));
-        }
-      }
     }
     // ------------------------------------------------------------ dK, dV out
     // TMEM loads are warp-collective: every lane takes part; only rows inside
-    // the sequence are stored.  dq_full of the last tile, waited above, already
-    // covers its dV / dK MMAs (the tensor core completes them in order).
+    // the sequence are stored.  dk_done of the last tile covers its dV too (the
+    // tensor core completes them in order); the math saw dp_ready of that tile,
+    // so dk_done is at most one phase behind.
     if (__all_sync(0xffffffffu, ok && !abort_flag) && it > 0)
       ok = mbar_wait_warp(&dk_done, (it - 1) & 1, &abort_flag, p.status, 607);
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
@@ -489,7 +442,6 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.D;
-  p.dq_acc = a.dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;

@@ -38,8 +38,7 @@ struct BwdArgs {
   const void* o;
   const void* dO;
   const float* lse;
-  float* D;       // fp32 [B,H,N]
-  float* dq_acc;  // fp32 [B,H,N,d]
+  float* D;  // fp32 [B,H,N]
   void* dq;
   void* dk;
   void* dv;
@@ -57,10 +56,6 @@ struct BwdArgs {
 // 128-byte swizzle, out-of-range rows read as zero.
 bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
-// Encodes a 3-D TMA descriptor over a [BH, N, d] fp32 tensor with a
-// 32-column x 128-row box and 128-byte swizzle (used for reduce-adds).
-bool encode_f32_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d);
-
 // Device address of the status block of the current device (no allocation:
 // it is a __device__ variable), or nullptr on failure.
 int* device_status();
@@ -69,7 +64,7 @@ int* device_status();
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
-cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_umma_probe(const void* a, const void* b, float* d, int M, int N, int K,

@@ -1,8 +1,7 @@
 // fa_bwd_noalloc: the bf16 backward pass for callers that cannot allocate
 // device memory.
 //
-// fa_bwd needs a workspace (the per-row D vector and an fp32 dQ accumulator)
-// that the caller allocates.  Some callers cannot do that: a plugin running
+// fa_bwd needs a workspace (the per-row D vector) that the caller allocates.  Some callers cannot do that: a plugin running
 // inside a host framework that has already reserved all device memory for its
 // own pool and forbids extensions from calling cudaMalloc, or latency-critical
 // code that must not call cudaMalloc/cudaFree because they can synchronize

@@ -85,8 +85,8 @@ typedef struct {
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, const fa_mask* mask, void* stream);
 
-/* Bytes of device workspace fa_bwd / fa_bwd_fp32 need: D (fp32 [B,H,N]) plus
- * an fp32 dQ accumulator [B,H,N,d], each padded to 256 bytes.  0 on bad sizes. */
+/* Bytes of device workspace fa_bwd / fa_bwd_fp32 need: D (fp32 [B,H,N]),
+ * padded to 256 bytes.  0 on bad sizes. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass, bf16.  Given the forward's inputs, its outputs o and lse,
@@ -98,26 +98,29 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * derivative, which the pages do not write out.
  *   workspace : device, >= fa_bwd_workspace_size(B,H,N,d) bytes, 16-byte
  *               aligned; contents on entry are ignored.
- * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq_convert on `stream`. */
+ * Runs fa_bwd_preprocess, fa_bwd_dkdv and fa_bwd_dq on `stream`. */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                  const fa_mask* mask, void* stream);
 
 /* The three steps of fa_bwd, exposed for timing each kernel on its own.
- * fa_bwd_preprocess: D[b,h,i] = sum_c dO[b,h,i,c] * O[b,h,i,c] (fp32), and
- *   sets dq_acc (fp32 [B,H,N,d]) to zero.
- * fa_bwd_dkdv: recomputes P and dS tile by tile, writes dk, dv (bf16) and
- *   adds scale * dS K into dq_acc.  D and dq_acc as left by the preprocess.
- * fa_bwd_dq_convert: dq (bf16) = dq_acc (fp32), round to nearest even. */
-fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, float* dq_acc, int B, int H,
-                            int N, int d, void* stream);
-fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
-                      const float* lse, const float* D, float* dq_acc, void* dk, void* dv, int B,
-                      int H, int N, int d, float scale, int causal, const fa_mask* mask,
-                      void* stream);
-fa_status fa_bwd_dq_convert(const float* dq_acc, void* dq, int B, int H, int N, int d,
+ * fa_bwd_preprocess: D[b,h,i] = sum_c dO[b,h,i,c] * O[b,h,i,c] (fp32 [B,H,N]).
+ * fa_bwd_dkdv: recomputes P and dS tile by tile for each 128-key tile and
+ *   writes dk, dv (bf16 [B,H,N,d]).  D as left by the preprocess.
+ * fa_bwd_dq: recomputes P and dS tile by tile for each 128-query tile and
+ *   writes dq (bf16 [B,H,N,d]); each row of dq is summed by one CTA in fp32,
+ *   so dq is the same bit for bit from run to run.
+ * fa_bwd_dkdv and fa_bwd_dq read the same inputs and write disjoint outputs:
+ *   they may run in either order, or concurrently on two streams. */
+fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
                             void* stream);
+fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
+                      const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
+                      int d, float scale, int causal, const fa_mask* mask, void* stream);
+fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
+                    const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
+                    const fa_mask* mask, void* stream);
 
 /* fp32 twins of fa_fwd / fa_bwd: identical argument meaning with fp32
  * tensors everywhere (CUDA cores, no tensor cores; for small fp32 workloads). */

@@ -59,7 +59,7 @@ def test_workspace_size(fa):
     B, H, N, d = 2, 3, 1000, 128
     rows = B * H * N
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) + r256(rows * d * 4)
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4)
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
 
@@ -120,11 +120,16 @@ def test_bwd_rejects_bad_arguments(fa, kw, code):
 
 
 def test_substeps_reject_bad_arguments(fa):
-    assert fa.lib.fa_bwd_preprocess(0, FAKE, FAKE, FAKE, 1, 1, 128, 64, None) == 1
-    assert fa.lib.fa_bwd_preprocess(FAKE, FAKE, FAKE, FAKE + 4, 1, 1, 128, 64, None) == 3
-    assert fa.lib.fa_bwd_dq_convert(FAKE, 0, 1, 1, 128, 64, None) == 1
-    assert fa.lib.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128,
+    assert fa.lib.fa_bwd_preprocess(0, FAKE, FAKE, 1, 1, 128, 64, None) == 1
+    assert fa.lib.fa_bwd_preprocess(FAKE, FAKE, FAKE + 2, 1, 1, 128, 64, None) == 3
+    assert fa.lib.fa_bwd_dkdv(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128,
                               80, 0.1, 0, None, None) == 2
+    assert fa.lib.fa_bwd_dq(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.1, 0, None,
+                            None) == 1
+    assert fa.lib.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 8, 1, 1, 128, 64, 0.1, 0,
+                            None, None) == 3
+    assert fa.lib.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.1, 2,
+                            None, None) == 1
     assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 64, 128, 64, 0, 0, 0, 0, None) == 2
     assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 1, 0, 1, 0, None) == 1
     assert fa.lib.fa_debug_wait_timeout(0, None) == 1

@@ -112,6 +112,19 @@ def test_forward_is_deterministic(fa):
     assert torch.equal(l1, l2)
 
 
+def test_backward_is_deterministic(fa):
+    # every dQ, dK, dV row is summed by one CTA in a fixed order: no atomics
+    case = random_case(2, 3, 1000, 128, seed=12)
+    t = to_device(case, "bf16")
+    scale = 128 ** -0.5
+    o, lse = fa.forward(t["q"], t["k"], t["v"], scale, True)
+    g1 = fa.backward(t["q"], t["k"], t["v"], o, t["do"], lse, scale, True)
+    g2 = fa.backward(t["q"], t["k"], t["v"], o, t["do"], lse, scale, True)
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # long workloads: sampled rows (O, lse, dQ on 256 query rows of every head;
 # dK, dV on 256 key rows of the first KEY_HEADS heads of batch 0, which need
