@@ -12,16 +12,18 @@
 // TMEM columns: S_0 [0,128) and S_1 [128,256) (S_j alternates between them;
 // after the math has read S_j, packed bf16 dS_j goes over its first half),
 // dP [256,384), dQ accumulator [384, 384+d).
-// Tensor-core order per key tile u (prologue: S_0, dP_0, S_1):
-//   dQ += dS_u K_u   A = dS_u from TMEM, B = K_u (MN-major)
+// Tensor-core work per key tile u (prologue: S_0, dP_0, S_1), once the math
+// has finished dS_u:
 //   dP_{u+1} = dO V_{u+1}^T
+//   dQ += dS_u K_u   A = dS_u from TMEM, B = K_u (MN-major)
 //   S_{u+2} = Q K_{u+2}^T   into the buffer dS_u occupied (after dQ_u is done)
-// so that while the math warps compute P_{u+1} and dS_{u+1}, the tensor core
-// has dQ_u, dP_{u+1} and S_{u+2} queued.
+// so that while the math warps compute P_{u+1} (S_{u+1} is ready) and then
+// dS_{u+1}, the tensor core has dP_{u+1}, dQ_u and S_{u+2} queued.
 //
-// Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// Roles (608 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // key columns [32w, 32w+32) of S / dP and d columns [w d/4, (w+1) d/4) of the
-// dQ read-out; warp 16 is the TMA producer; warp 17 issues the MMAs.
+// dQ read-out; warp 16 is the TMA producer; warps 17 and 18 issue the MMAs
+// (S, dP and dQ respectively).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -46,7 +48,7 @@ struct DqCfg {
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
   static constexpr int kMathWarps = 16;
-  static constexpr int kThreads = kMathWarps * 32 + 64;
+  static constexpr int kThreads = kMathWarps * 32 + 96;  // + producer, two MMA issuers
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-out
 };
 
@@ -83,10 +85,19 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, dp_full, ds_ready, dq_done, drain;
-  __shared__ uint64_t s_full[2];
-  __shared__ uint64_t k_full[C::kKStages], k_empty[C::kKStages];
-  __shared__ uint64_t v_full[C::kVStages], v_empty[C::kVStages];
+  __shared__ uint64_t q_full, drain, drain_a;
+  // per S buffer: S_u is in buffer u & 1 (s_full), dS_u written over it
+  // (ds_ready).  Both issuers wait on ds_ready; with one barrier per buffer the
+  // next phase of the barrier a thread waits on needs S_{u+2}, hence dQ_u,
+  // hence that wait: no waiter can fall a phase behind.
+  __shared__ uint64_t s_full[2], ds_ready[2];
+  // dq_done[s] completes when dQ of the key tile in K stage s is done: it frees
+  // the stage and the S buffer that held that tile's dS; dp_full[s] completes
+  // when dP of the key tile in V stage s is done: it frees the stage and tells
+  // the math dP is ready.  One commit each per key tile; per-stage barriers
+  // keep every waiter within one phase.
+  __shared__ uint64_t k_full[C::kKStages], dq_done[C::kKStages];
+  __shared__ uint64_t v_full[C::kVStages], dp_full[C::kVStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -105,18 +116,19 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&dp_full, 1);
-    mbar_init(&ds_ready, C::kMathWarps);  // one arrival per math warp
-    mbar_init(&dq_done, 1);
     mbar_init(&drain, 1);
-    for (int x = 0; x < 2; ++x) mbar_init(&s_full[x], 1);
+    mbar_init(&drain_a, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&ds_ready[x], C::kMathWarps);  // one arrival per math warp
+    }
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
+      mbar_init(&dq_done[s], 1);
     }
     for (int s = 0; s < C::kVStages; ++s) {
       mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&dp_full[s], 1);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -153,14 +165,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       for (int j = jfirst; j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
         prefetch_upto(u + 1 + C::kPrefetchTiles);
         const int ks = u % C::kKStages, vs = u % C::kVStages;
-        if (!mbar_wait(&k_empty[ks], ((u / C::kKStages) & 1) ^ 1, &abort_flag, p.status, 701))
+        if (!mbar_wait(&dq_done[ks], ((u / C::kKStages) & 1) ^ 1, &abort_flag, p.status, 701))
           break;
         mbar_expect_tx(&k_full[ks], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_3d(&tmK, &k_full[ks], smem + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
                       c * 64, j * 128, bh);
         ++kcount[ks];
-        if (!mbar_wait(&v_empty[vs], ((u / C::kVStages) & 1) ^ 1, &abort_flag, p.status, 702))
+        if (!mbar_wait(&dp_full[vs], ((u / C::kVStages) & 1) ^ 1, &abort_flag, p.status, 702))
           break;
         mbar_expect_tx(&v_full[vs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
@@ -175,8 +187,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       for (int s = 0; s < C::kVStages; ++s)
         if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
     }
-  } else if (warp == C::kMathWarps + 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == C::kMathWarps + 1 || warp == C::kMathWarps + 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads, one per dependency chain (an MMA costs its issuing
+    // thread about as long as the tensor core takes to run it, so one thread
+    // waiting on one chain would starve the other):
+    //   A (warp 17): S and dP -- gated by the loads, the math's reads of dP
+    //                and dQ's read of the S buffer
+    //   B (warp 18): dQ       -- gated by the math (dS)
+    const bool issuer_a = warp == C::kMathWarps + 1;
     if (lane == 0 && any) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);    // dQ (A in TMEM)
@@ -209,43 +228,55 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
           mma_ss(tmem + C::kColDP, dDO_k + off, dV_k + off, idesc_s, kk > 0);
         }
-        mma_commit(&dp_full);
-        mma_commit(&v_empty[vs]);
+        mma_commit(&dp_full[vs]);
         return true;
       };
-      bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 800);
-      const int j1 = ktiles.next(jfirst + 1);
-      if (ok) ok = issue_s(0, 0);
-      if (ok) ok = issue_dp(0);
-      if (ok && j1 < ktiles.jend) ok = issue_s(1, 1);
+      bool ok = true;
       int u = 0;
-      for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
-        const int x = u & 1;
-        ok = mbar_wait(&ds_ready, u & 1, &abort_flag, p.status, 803);
-        if (!ok) break;
-        tc_fence_after();
-        // dQ += dS_u K_u: dS_u packed in the first half of buffer x (warpgroup
-        // w's keys [32w, 32w+32) in columns [32w, 32w+16)); K_u read MN-major
-        const uint64_t dK_mn = sdesc_sw128(sK + (u % C::kKStages) * C::kTileBytes, C::kChunkBytes, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + C::kColDQ, tmem + C::kColS + 128 * x + 32 * (kk >> 1) + 8 * (kk & 1),
-                 dK_mn + kk * (2048 >> 4), idesc_dq, (u > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&dq_done);
-        mma_commit(&k_empty[u % C::kKStages]);
-        const int jn = ktiles.next(j + 1);
-        if (jn < ktiles.jend) {
-          ok = issue_dp(u + 1);  // the math has read dP_u (ds_ready)
-          if (!ok) break;
-          if (ktiles.next(jn + 1) < ktiles.jend) {
-            // buffer x is free once dQ_u, the last reader of dS_u, is done
-            ok = mbar_wait(&dq_done, u & 1, &abort_flag, p.status, 804);
-            if (ok) ok = issue_s(u + 2, x);
+      if (issuer_a) {
+        // A: S and dP.  S_{u+2} overwrites the buffer of dS_u: after dQ_u (B)
+        ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 800);
+        const int j1 = ktiles.next(jfirst + 1);
+        if (ok) ok = issue_s(0, 0);
+        if (ok) ok = issue_dp(0);
+        if (ok && j1 < ktiles.jend) ok = issue_s(1, 1);
+        for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+          const int jn = ktiles.next(j + 1);
+          if (jn >= ktiles.jend) break;
+          // dP_{u+1} once the math has read dP_u (ds_ready)
+          ok = mbar_wait(&ds_ready[u & 1], (u >> 1) & 1, &abort_flag, p.status, 803);
+          if (ok) ok = issue_dp(u + 1);
+          if (ok && ktiles.next(jn + 1) < ktiles.jend) {
+            ok = mbar_wait(&dq_done[u % C::kKStages], (u / C::kKStages) & 1, &abort_flag, p.status,
+                           804);
+            if (ok) ok = issue_s(u + 2, u & 1);
           }
         }
+      } else {
+        // B: dQ += dS_u K_u once the math has written dS_u (ds_ready).  dS_u is
+        // packed in the first half of buffer u & 1 (warpgroup w's keys
+        // [32w, 32w+32) in columns [32w, 32w+16)); K_u is read MN-major
+        for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+          const int ks = u % C::kKStages;
+          ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 805);
+          if (ok) ok = mbar_wait(&ds_ready[u & 1], (u >> 1) & 1, &abort_flag, p.status, 806);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dK_mn = sdesc_sw128(sK + ks * C::kTileBytes, C::kChunkBytes, 1024);
+          const uint32_t tA = tmem + C::kColS + 128 * (u & 1);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + C::kColDQ, tA + 32 * (kk >> 1) + 8 * (kk & 1), dK_mn + kk * (2048 >> 4),
+                   idesc_dq, (u > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&dq_done[ks]);
+        }
       }
-      mma_commit(&drain);
-      mbar_drain(&drain, 0);
+      // each issuer's MMAs are complete once its drain barrier flips; B's last
+      // dQ follows every MMA of A (it waited for the last dP through
+      // ds_ready), so `drain` alone tells the math that all are done
+      uint64_t* my_drain = issuer_a ? &drain_a : &drain;
+      mma_commit(my_drain);
+      mbar_drain(my_drain, 0);
     }
   } else {
     // ------------------------------------------------------------ math warpgroups
@@ -293,7 +324,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int e = 0; e < 32; ++e)
           if (e >= lim) pf[e] = 0.f;
       }
-      ok = mbar_wait_warp(&dp_full, u & 1, &abort_flag, p.status, 902);
+      ok = mbar_wait_warp(&dp_full[u % C::kVStages], (u / C::kVStages) & 1, &abort_flag, p.status,
+                          902);
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[16];
@@ -313,12 +345,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       FA_TMEM_ST16(tS, dsp);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&ds_ready);
+      mbar_arrive_warp(&ds_ready[x]);
     }
     // ------------------------------------------------------------ epilogue
+    // `drain` completes once, after the issuer's last MMA: unlike the per-tile
+    // barriers, whose earlier phases may still be pending here, it cannot alias
     bool have = false;
     if (__all_sync(0xffffffffu, ok && !abort_flag) && u > 0)
-      have = mbar_wait_warp(&dq_done, (u - 1) & 1, &abort_flag, p.status, 903);
+      have = mbar_wait_warp(&drain, 0, &abort_flag, p.status, 903);
     if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
       tc_fence_after();
       uint32_t r[C::kDSlice];

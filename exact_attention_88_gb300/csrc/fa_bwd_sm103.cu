@@ -24,9 +24,10 @@
 //   dK += dS^T Q_i A from TMEM
 // so the next tile's S^T queues behind dK without waiting for it.
 //
-// Roles (576 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// Roles (608 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4)
-// of dK, dV; warp 16 is the TMA producer; warp 17 issues the MMAs.
+// of dK, dV; warp 16 is the TMA producer; warps 17 and 18 issue the MMAs
+// (S^T, dP^T and dV, dK respectively).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -52,7 +53,7 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr int kMathWarps = 16;
   static constexpr int kMathThreads = kMathWarps * 32;
-  static constexpr int kThreads = kMathThreads + 64;
+  static constexpr int kThreads = kMathThreads + 96;  // + producer, two MMA issuers
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the dK / dV read-out
 };
 
@@ -102,8 +103,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, dv_done, dk_done, stats_ready,
-      drain;
+  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, stats_ready, drain, drain_a;
+  // q_empty[s] completes when dK of the tile in Q stage s is done: it both frees
+  // the stage and tells the issuer that dS^T (in the dP^T columns) was read;
+  // do_empty[s] likewise for dV, the dO stage and P^T (in the S^T columns).
+  // One commit per tile each; per-stage barriers keep every waiter within
+  // one phase.
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
   __shared__ __align__(16) float s_nl2[128];  // -lse2 of the tile's query rows
@@ -128,10 +133,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&dp_ready, 1);
     mbar_init(&p_ready, C::kMathWarps);  // one arrival per math warp
     mbar_init(&ds_ready, C::kMathWarps);
-    mbar_init(&dv_done, 1);
-    mbar_init(&dk_done, 1);
     mbar_init(&stats_ready, 4);
     mbar_init(&drain, 1);
+    mbar_init(&drain_a, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);  // dK, the last reader of Q_i, is done
@@ -198,8 +202,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int s = 0; s < C::kDOStages; ++s)
         if (dcount[s]) mbar_drain(&do_full[s], (dcount[s] - 1) & 1);
     }
-  } else if (warp == C::kMathWarps + 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == C::kMathWarps + 1 || warp == C::kMathWarps + 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing threads, one per dependency chain, so that a wait on one
+    // chain never holds back the other's MMAs (an MMA costs its issuing thread
+    // about as long as the tensor core takes to run it):
+    //   A (warp 17): S^T and dP^T -- gated by the loads and by the previous
+    //                tile's dV / dK (the readers of the columns they overwrite)
+    //   B (warp 18): dV and dK    -- gated by the math (P^T, dS^T)
+    const bool issuer_a = warp == C::kMathWarps + 1;
     if (lane == 0 && iend > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
@@ -209,64 +220,75 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // its byte offset >> 4 to the start-address field (every buffer lies
       // below 256 KB, so the 14-bit field never carries)
       const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
-      bool ok = mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
+      bool ok = !issuer_a || mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
-        const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dQ_mn = sdesc_sw128(sQ, C::kChunkBytes, 1024);
-        const uint64_t dDO_k = sdesc_sw128(sDO, 16, 1024);
-        const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
         ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
-        // P^T of the previous tile sits in the S^T columns until dV is done
-        if (ok && it > 0) ok = mbar_wait(&dv_done, (it - 1) & 1, &abort_flag, p.status, 503);
         if (!ok) break;
-        tc_fence_after();
-        // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
+        if (issuer_a) {
+          const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dDO_k = sdesc_sw128(sDO, 16, 1024);
+          // P^T of the previous tile sits in the S^T columns until its dV is done
+          if (it > 0)
+            ok = mbar_wait(&do_empty[(it - 1) % C::kDOStages], ((it - 1) / C::kDOStages) & 1,
+                           &abort_flag, p.status, 503);
+          if (!ok) break;
+          tc_fence_after();
+          // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
+          }
+          mma_commit(&s_ready);
+          // dS^T of the previous tile sits in the dP^T columns until its dK is done
+          if (it > 0)
+            ok = mbar_wait(&q_empty[(it - 1) % C::kQStages], ((it - 1) / C::kQStages) & 1,
+                           &abort_flag, p.status, 504);
+          if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
+          if (!ok) break;
+          tc_fence_after();
+          // dP^T = V dO^T
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tmem + C::kColDP, dV_k + koff, dDO_k + koff, idesc_s, ks > 0);
+          }
+          mma_commit(&dp_ready);
+        } else {
+          const uint64_t dQ_mn = sdesc_sw128(sQ, C::kChunkBytes, 1024);
+          const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
+          const uint32_t acc = it > 0 ? 1u : 0u;
+          ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 508);
+          if (ok) ok = mbar_wait(&p_ready, it & 1, &abort_flag, p.status, 505);
+          if (!ok) break;
+          tc_fence_after();
+          // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed in
+          // columns [32w, 32w+16) of the S^T region)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
+                   dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
+          mma_commit(&do_empty[ds]);
+          ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
+          if (!ok) break;
+          tc_fence_after();
+          // dK += dS^T Q (dS^T in TMEM: warpgroup w's columns packed in
+          // [32w, 32w+16) of the dP^T region)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tmem + C::kColDK, tmem + C::kColDP + 32 * (ks >> 1) + 8 * (ks & 1),
+                   dQ_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
+          mma_commit(&q_empty[qs]);
         }
-        mma_commit(&s_ready);
-        // dS^T of the previous tile sits in the dP^T columns until dK is done
-        if (it > 0) ok = mbar_wait(&dk_done, (it - 1) & 1, &abort_flag, p.status, 504);
-        if (ok) ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 506);
-        if (!ok) break;
-        tc_fence_after();
-        // dP^T = V dO^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
-          mma_ss(tmem + C::kColDP, dV_k + koff, dDO_k + koff, idesc_s, ks > 0);
-        }
-        mma_commit(&dp_ready);
-        ok = mbar_wait(&p_ready, it & 1, &abort_flag, p.status, 505);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t acc = it > 0 ? 1u : 0u;
-        // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed in
-        // columns [32w, 32w+16) of the S^T region)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
-                 dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
-        mma_commit(&dv_done);
-        mma_commit(&do_empty[ds]);
-        ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
-        if (!ok) break;
-        tc_fence_after();
-        // dK += dS^T Q (dS^T in TMEM: warpgroup w's columns packed in [32w, 32w+16)
-        // of the dP^T region)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + C::kColDK, tmem + C::kColDP + 32 * (ks >> 1) + 8 * (ks & 1),
-                 dQ_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
-        mma_commit(&dk_done);
-        mma_commit(&q_empty[qs]);
       }
-      mma_commit(&drain);
-      mbar_drain(&drain, 0);
+      // each issuer's MMAs are complete once its drain barrier flips; B's last
+      // MMA (dK) follows every MMA of A (it waited for the last dP^T through
+      // ds_ready), so `drain` alone tells the math that all are done
+      uint64_t* my_drain = issuer_a ? &drain_a : &drain;
+      mma_commit(my_drain);
+      mbar_drain(my_drain, 0);
     }
   } else {
     // ------------------------------------------------------------ math warpgroups
@@ -394,11 +416,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     // ------------------------------------------------------------ dK, dV out
     // TMEM loads are warp-collective: every lane takes part; only rows inside
-    // the sequence are stored.  dk_done of the last tile covers its dV too (the
-    // tensor core completes them in order); the math saw dp_ready of that tile,
-    // so dk_done is at most one phase behind.
+    // the sequence are stored.  `drain` completes once, after the issuer's
+    // last MMA (a per-tile barrier's parity could alias an earlier phase).
     if (__all_sync(0xffffffffu, ok && !abort_flag) && it > 0)
-      ok = mbar_wait_warp(&dk_done, (it - 1) & 1, &abort_flag, p.status, 607);
+      ok = mbar_wait_warp(&drain, 0, &abort_flag, p.status, 607);
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
     if (live) {
       tc_fence_after();
