@@ -15,7 +15,7 @@
 // queued.  TMEM columns: S_A / P_A [0,128), O_A [128, 128+d), S_B / P_B
 // [256, 384), O_B [384, 384+d).
 //
-// Roles (320 threads):
+// Roles (352 threads):
 //   warps 0-3, 4-7  softmax of tile A, B: thread t owns row t (TMEM lane t);
 //                   reads its 128 scores (max, then exponentials), masks,
 //                   updates m and l, writes P~ = 2^(c S - m) as packed bf16
@@ -23,7 +23,7 @@
 //                   rescales O in TMEM when m grew by more than 8 in log2 units
 //                   (lazy rescale), and at the end writes O / l and lse.
 //   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
-//   warp 9          MMA issuer (one thread).
+//   warps 9, 10     MMA issuers for tile A, B (one thread each).
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
 #include "fa_common.cuh"
 #include "fa_internal.h"
@@ -46,7 +46,7 @@ struct FwdCfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kSmem = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
   static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 320;
+  static constexpr int kThreads = 352;
 };
 
 struct FwdParams {
@@ -168,14 +168,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
 }
 
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, drain;
+  __shared__ uint64_t q_full, drain[2];
   __shared__ uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
   __shared__ uint64_t k_full[C::kStages], v_full[C::kStages], k_empty[C::kStages],
       v_empty[C::kStages];
@@ -202,7 +202,8 @@ __global__ void __launch_bounds__(320, 1)
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
-    mbar_init(&drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       mbar_init(&p_full[x], 128);
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(320, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+      mbar_init(&k_empty[s], 2);  // one commit from each issuer
+      mbar_init(&v_empty[s], 2);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -264,62 +265,67 @@ __global__ void __launch_bounds__(320, 1)
         if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 9 || warp == 10) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile (warp 9: A, warp 10: B): an MMA costs
+    // its issuing thread about as long as the tensor core takes to run it, so
+    // a single thread waiting on one tile's softmax would starve the other
+    // tile's MMAs.  Both walk the key tiles either tile sees and release each
+    // K / V stage with a commit of their own (the stage barriers count two).
+    // (B runs even without a tile B: it still owes its commit for every stage)
+    const int x = warp - 9;
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
-      const uint32_t sQ = smem_addr(smem + C::kOffQ);
+      const uint64_t dQx = sdesc_sw128(smem_addr(smem + C::kOffQ + x * C::kTileBytes), 16, 1024);
       const uint32_t sK = smem_addr(smem + C::kOffK);
       const uint32_t sV = smem_addr(smem + C::kOffV);
-      int cnt[2] = {0, 0};  // key tiles finished per query tile
+      const uint32_t tS = tmem + 256 * x, tO = tS + 128;
+      int cnt = 0;  // key tiles this query tile has finished
       bool ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 201);
       int u = 0;
       for (int j = tiles.next(0); ok && j < tiles.end(); j = tiles.next(j + 1), ++u) {
         const int st = u % C::kStages;
         const uint32_t ph = (u / C::kStages) & 1;
-        const bool vis[2] = {tiles.vis_a(j), tiles.vis_b(j)};
+        const bool vis = x == 0 ? tiles.vis_a(j) : tiles.vis_b(j);
+        // Each issuer waits for the stage's load even when its tile does not
+        // see key tile j: a commit made without it could run a whole ring ahead
+        // and count toward the stage's current phase.
         ok = mbar_wait(&k_full[st], ph, &abort_flag, p.status, 202);
-        const uint32_t kbase = sK + st * C::kTileBytes, vbase = sV + st * C::kTileBytes;
-        // S_x = Q_x K_j^T for each tile that sees j (after x's previous P V:
-        // its P sits in the S columns until then)
-        for (int x = 0; ok && x < 2; ++x) {
-          if (!vis[x]) continue;
-          if (cnt[x] > 0) ok = mbar_wait(&o_done[x], (cnt[x] - 1) & 1, &abort_flag, p.status, 203 + x);
+        if (!ok) break;
+        if (vis) {
+          // S_x = Q_x K_j^T, after x's previous P V (its P sits in the S columns)
+          if (cnt > 0) ok = mbar_wait(&o_done[x], (cnt - 1) & 1, &abort_flag, p.status, 203 + x);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t qbase = sQ + x * C::kTileBytes;
+          const uint64_t dK = sdesc_sw128(sK + st * C::kTileBytes, 16, 1024);
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * C::kChunkBytes + (ks & 3) * 32;
-            mma_ss(tmem + 256 * x, sdesc_sw128(qbase + off, 16, 1024),
-                   sdesc_sw128(kbase + off, 16, 1024), idesc_qk, ks > 0 ? 1u : 0u);
+            const uint32_t off = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+            mma_ss(tS, dQx + off, dK + off, idesc_qk, ks > 0 ? 1u : 0u);
           }
           mma_commit(&s_full[x]);
         }
-        if (!ok) break;
         mma_commit(&k_empty[st]);
         ok = mbar_wait(&v_full[st], ph, &abort_flag, p.status, 207);
-        // O_x += P_x V_j, P_x read from TMEM (packed, 8 columns per 16 keys)
-        for (int x = 0; ok && x < 2; ++x) {
-          if (!vis[x]) continue;
-          ok = mbar_wait(&p_full[x], cnt[x] & 1, &abort_flag, p.status, 205 + x);
+        if (!ok) break;
+        if (vis) {
+          // O_x += P_x V_j, P_x read from TMEM (packed, 8 columns per 16 keys)
+          ok = mbar_wait(&p_full[x], cnt & 1, &abort_flag, p.status, 205 + x);
           if (!ok) break;
           tc_fence_after();
+          const uint64_t dV = sdesc_sw128(sV + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tmem + 256 * x + 128, tmem + 256 * x + ks * 8,
-                   sdesc_sw128(vbase + ks * 2048, C::kChunkBytes, 1024), idesc_pv,
-                   (cnt[x] > 0 || ks > 0) ? 1u : 0u);
+            mma_ts(tO, tS + ks * 8, dV + ks * (2048 >> 4), idesc_pv, (cnt > 0 || ks > 0) ? 1u : 0u);
           mma_commit(&o_done[x]);
-          ++cnt[x];
+          ++cnt;
         }
-        if (!ok) break;
         mma_commit(&v_empty[st]);
       }
-      // all MMAs issued by this thread are complete once `drain` flips
-      mma_commit(&drain);
-      mbar_drain(&drain, 0);
+      // all MMAs issued by this thread are complete once its drain flips
+      mma_commit(&drain[x]);
+      mbar_drain(&drain[x], 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
