@@ -176,7 +176,10 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t q_full, drain[2];
-  __shared__ uint64_t s_full[2], p_full[2], o_done[2];  // per query tile
+  __shared__ uint64_t s_full[2], p_full[2], o_done[2], turn[2];  // per query tile
+  // turn[x]: tile x's softmax may run.  The two softmax warpgroups take turns
+  // key tile by key tile (A, B, A, B, ...), so that each runs alone on the
+  // SMSPs while the tensor core works for the other tile.
   __shared__ uint64_t k_full[C::kStages], v_full[C::kStages], k_empty[C::kStages],
       v_empty[C::kStages];
   __shared__ uint32_t tmem_slot;
@@ -206,7 +209,8 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&drain[1], 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
+      mbar_init(&p_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&turn[x], 4);
       mbar_init(&o_done[x], 1);
     }
     for (int s = 0; s < C::kStages; ++s) {
@@ -339,16 +343,27 @@ __global__ void __launch_bounds__(352, 1)
     bool ok = true;
     const bool live_tile = x == 0 || has_b;
     if (live_tile) {
-      for (int j = tiles.next(0); j < tiles.end(); j = tiles.next(j + 1)) {
-        if (!(x == 0 ? tiles.vis_a(j) : tiles.vis_b(j))) continue;
-        ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
-        if (!ok) break;
-        tc_fence_after();
-        softmax_tile(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0, p.scale_log2, n == 0, m,
-                     l);
-        tc_fence_before();
-        mbar_arrive(&p_full[x]);
-        ++n;
+      int u = 0;  // key tiles either tile sees, in order
+      for (int j = tiles.next(0); j < tiles.end(); j = tiles.next(j + 1), ++u) {
+        // A's turn for key tile u comes after B's for u - 1, B's after A's for
+        // u (each turn barrier's next phase needs this warpgroup's own next
+        // pass, so no waiter can fall a phase behind).  Without a tile B, A
+        // runs on its own.
+        if (has_b && (x == 1 || u > 0)) {
+          ok = mbar_wait_warp(&turn[x], (x == 1 ? u : u - 1) & 1, &abort_flag, p.status, 305 + x);
+          if (!ok) break;
+        }
+        if (x == 0 ? tiles.vis_a(j) : tiles.vis_b(j)) {
+          ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
+          if (!ok) break;
+          tc_fence_after();
+          softmax_tile(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0, p.scale_log2, n == 0,
+                       m, l);
+          tc_fence_before();
+          mbar_arrive_warp(&p_full[x]);
+          ++n;
+        }
+        if (has_b) mbar_arrive_warp(&turn[x ^ 1]);  // the other tile's turn
       }
     }
     // ------------------------------------------------------------ epilogue
