@@ -35,6 +35,11 @@ from workloads import WORKLOADS, generate, flops  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal, 1 GB300) and % of dense bf16 peak"
 DEFAULT_WORKLOAD = "long_causal_d128"
+# DRAM bytes (read + write) of one fa_bwd_dkdv launch on the default workload,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# current version of that kernel; set to None whenever the kernel changes
+# until it is captured again.
+DKDV_DRAM_BYTES = {"long_causal_d128": 1.046e9}
 
 
 def measured_peaks():
@@ -247,7 +252,8 @@ def run_gpu(args, rank, world, local_rank):
             "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4),
             "peak_source": "bf16 burst, %s (MEASURED_PEAKS.json)" % peak_kind,
-            "traffic": None,
+            "traffic": DKDV_DRAM_BYTES.get(w.name),
+            "traffic_unit": "bytes per launch (ncu capture)",
             "flops_per_launch": dkdv_flops,
         },
         "fwd_roofline": {"kernel": "fa_fwd", "achieved": round(fwd_achieved, 2),
