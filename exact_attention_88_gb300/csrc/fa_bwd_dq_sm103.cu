@@ -9,21 +9,19 @@
 // textbook derivative of the definition; the pages do not print them.)
 //
 // Query rows sit on the TMEM lanes, so lse and D are one scalar per thread.
-// TMEM columns: S_0 [0,128) and S_1 [128,256) (S_j alternates between them;
-// after the math has read S_j, packed bf16 dS_j goes over its first half),
-// dP [256,384), dQ accumulator [384, 384+d).
-// Tensor-core work per key tile u (prologue: S_0, dP_0, S_1), once the math
-// has finished dS_u:
-//   dP_{u+1} = dO V_{u+1}^T
-//   dQ += dS_u K_u   A = dS_u from TMEM, B = K_u (MN-major)
-//   S_{u+2} = Q K_{u+2}^T   into the buffer dS_u occupied (after dQ_u is done)
-// so that while the math warps compute P_{u+1} (S_{u+1} is ready) and then
-// dS_{u+1}, the tensor core has dP_{u+1}, dQ_u and S_{u+2} queued.
+// TMEM columns: S [0,128), dP_0 [128,256) and dP_1 [256,384) (dP_u alternates
+// between them; once the math has read dP_u, packed bf16 dS_u goes over its
+// first half), dQ accumulator [384, 384+d).  Per key tile u the math computes
+// P_u from S_u (kept in registers), then dS_u; the tensor core work is
+//   S_{u+1} = Q K_{u+1}^T   as soon as the math has read S_u
+//   dP_{u+2} = dO V_{u+2}^T once dQ_u has read dS_u from that dP buffer
+//   dQ += dS_u K_u          A = dS_u from TMEM, B = K_u (MN-major)
+// so every MMA the math waits for was issued about a key tile earlier.
 //
-// Roles (608 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// Roles (640 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // key columns [32w, 32w+32) of S / dP and d columns [w d/4, (w+1) d/4) of the
-// dQ read-out; warp 16 is the TMA producer; warps 17 and 18 issue the MMAs
-// (S, dP and dQ respectively).
+// dQ read-out; warp 16 is the TMA producer; warps 17, 18, 19 issue S, dP and
+// dQ (one thread each).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -46,9 +44,9 @@ struct DqCfg {
   static constexpr int kOffV = kOffK + kKStages * kTileBytes;
   static constexpr int kSmem = kOffV + kVStages * kTileBytes + 1024;
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 384;  // dP_b at kColDP + 128 b
   static constexpr int kMathWarps = 16;
-  static constexpr int kThreads = kMathWarps * 32 + 96;  // + producer, two MMA issuers
+  static constexpr int kThreads = kMathWarps * 32 + 128;  // + producer, three MMA issuers
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-out
 };
 
@@ -85,17 +83,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t q_full, drain, drain_a;
-  // per S buffer: S_u is in buffer u & 1 (s_full), dS_u written over it
-  // (ds_ready).  Both issuers wait on ds_ready; with one barrier per buffer the
-  // next phase of the barrier a thread waits on needs S_{u+2}, hence dQ_u,
-  // hence that wait: no waiter can fall a phase behind.
-  __shared__ uint64_t s_full[2], ds_ready[2];
-  // dq_done[s] completes when dQ of the key tile in K stage s is done: it frees
-  // the stage and the S buffer that held that tile's dS; dp_full[s] completes
-  // when dP of the key tile in V stage s is done: it frees the stage and tells
-  // the math dP is ready.  One commit each per key tile; per-stage barriers
-  // keep every waiter within one phase.
+  __shared__ uint64_t q_full, s_full, s_free, drain, drain_s, drain_p;
+  // ds_ready[b]: dS of the key tile whose dP is in buffer b is written (over
+  // that buffer).  dp_full[b]: dP of the key tile in V stage b (= dP buffer b)
+  // is done; it frees the stage too.  dq_done[s]: dQ of the key tile in K
+  // stage s is done; it frees the stage and the dP buffer that held its dS.
+  // One commit each per key tile; per-buffer / per-stage barriers keep every
+  // waiter within one phase (the next phase of each needs that waiter's own
+  // progress first).
+  __shared__ uint64_t ds_ready[2];
   __shared__ uint64_t k_full[C::kKStages], dq_done[C::kKStages];
   __shared__ uint64_t v_full[C::kVStages], dp_full[C::kVStages];
   __shared__ uint32_t tmem_slot;
@@ -116,12 +112,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
+    mbar_init(&s_full, 1);
+    mbar_init(&s_free, C::kMathWarps);  // one arrival per math warp
     mbar_init(&drain, 1);
-    mbar_init(&drain_a, 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&ds_ready[x], C::kMathWarps);  // one arrival per math warp
-    }
+    mbar_init(&drain_s, 1);
+    mbar_init(&drain_p, 1);
+    for (int x = 0; x < 2; ++x) mbar_init(&ds_ready[x], C::kMathWarps);
     for (int s = 0; s < C::kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&dq_done[s], 1);
@@ -187,15 +183,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       for (int s = 0; s < C::kVStages; ++s)
         if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
     }
-  } else if (warp == C::kMathWarps + 1 || warp == C::kMathWarps + 2) {
+  } else if (warp >= C::kMathWarps + 1) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads, one per dependency chain (an MMA costs its issuing
-    // thread about as long as the tensor core takes to run it, so one thread
-    // waiting on one chain would starve the other):
-    //   A (warp 17): S and dP -- gated by the loads, the math's reads of dP
-    //                and dQ's read of the S buffer
-    //   B (warp 18): dQ       -- gated by the math (dS)
-    const bool issuer_a = warp == C::kMathWarps + 1;
+    // One issuing thread per MMA kind (an MMA costs its issuing thread about as
+    // long as the tensor core takes to run it, so a thread waiting on one
+    // dependency would starve the others):
+    //   warp 17: S_u    -- after the math has read S_{u-1} (s_free)
+    //   warp 18: dP_u   -- after dQ_{u-2} has read the dS in buffer u & 1
+    //   warp 19: dQ_u   -- after the math has written dS_u (ds_ready)
+    const int role = warp - (C::kMathWarps + 1);
     if (lane == 0 && any) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);  // S, dP
       constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);    // dQ (A in TMEM)
@@ -204,66 +200,53 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const uint64_t dQ_k = sdesc_sw128(smem_addr(smem + C::kOffQ), 16, 1024);
       const uint64_t dDO_k = sdesc_sw128(smem_addr(smem + C::kOffDO), 16, 1024);
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
-      // S_u = Q K_u^T into buffer x; dP_u = dO V_u^T
-      auto issue_s = [&](int u, int x) -> bool {
-        const int ks = u % C::kKStages;
-        if (!mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 801)) return false;
-        tc_fence_after();
-        const uint64_t dK_k = sdesc_sw128(sK + ks * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::kColS + 128 * x, dQ_k + off, dK_k + off, idesc_s, kk > 0);
-        }
-        mma_commit(&s_full[x]);
-        return true;
-      };
-      auto issue_dp = [&](int u) -> bool {
-        const int vs = u % C::kVStages;
-        if (!mbar_wait(&v_full[vs], (u / C::kVStages) & 1, &abort_flag, p.status, 802)) return false;
-        tc_fence_after();
-        const uint64_t dV_k = sdesc_sw128(sV + vs * C::kTileBytes, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + C::kColDP, dDO_k + off, dV_k + off, idesc_s, kk > 0);
-        }
-        mma_commit(&dp_full[vs]);
-        return true;
-      };
       bool ok = true;
       int u = 0;
-      if (issuer_a) {
-        // A: S and dP.  S_{u+2} overwrites the buffer of dS_u: after dQ_u (B)
+      if (role == 0) {
         ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 800);
-        const int j1 = ktiles.next(jfirst + 1);
-        if (ok) ok = issue_s(0, 0);
-        if (ok) ok = issue_dp(0);
-        if (ok && j1 < ktiles.jend) ok = issue_s(1, 1);
-        for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
-          const int jn = ktiles.next(j + 1);
-          if (jn >= ktiles.jend) break;
-          // dP_{u+1} once the math has read dP_u (ds_ready)
-          ok = mbar_wait(&ds_ready[u & 1], (u >> 1) & 1, &abort_flag, p.status, 803);
-          if (ok) ok = issue_dp(u + 1);
-          if (ok && ktiles.next(jn + 1) < ktiles.jend) {
-            ok = mbar_wait(&dq_done[u % C::kKStages], (u / C::kKStages) & 1, &abort_flag, p.status,
-                           804);
-            if (ok) ok = issue_s(u + 2, u & 1);
-          }
-        }
-      } else {
-        // B: dQ += dS_u K_u once the math has written dS_u (ds_ready).  dS_u is
-        // packed in the first half of buffer u & 1 (warpgroup w's keys
-        // [32w, 32w+32) in columns [32w, 32w+16)); K_u is read MN-major
         for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
           const int ks = u % C::kKStages;
-          ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 805);
-          if (ok) ok = mbar_wait(&ds_ready[u & 1], (u >> 1) & 1, &abort_flag, p.status, 806);
+          if (u > 0) ok = mbar_wait(&s_free, (u - 1) & 1, &abort_flag, p.status, 801);
+          if (ok) ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 802);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dK_k = sdesc_sw128(sK + ks * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kColS, dQ_k + off, dK_k + off, idesc_s, kk > 0);
+          }
+          mma_commit(&s_full);
+        }
+      } else if (role == 1) {
+        ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 803);
+        for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+          const int vs = u % C::kVStages;  // = dP buffer
+          if (u >= 2)
+            ok = mbar_wait(&dq_done[(u - 2) % C::kKStages], ((u - 2) / C::kKStages) & 1,
+                           &abort_flag, p.status, 804);
+          if (ok) ok = mbar_wait(&v_full[vs], (u / C::kVStages) & 1, &abort_flag, p.status, 805);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dV_k = sdesc_sw128(sV + vs * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kColDP + 128 * vs, dDO_k + off, dV_k + off, idesc_s, kk > 0);
+          }
+          mma_commit(&dp_full[vs]);
+        }
+      } else {
+        // dQ += dS_u K_u: dS_u packed in the first half of dP buffer u & 1
+        // (warpgroup w's keys [32w, 32w+32) in columns [32w, 32w+16))
+        for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+          const int ks = u % C::kKStages;
+          ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 806);
+          if (ok) ok = mbar_wait(&ds_ready[u & 1], (u >> 1) & 1, &abort_flag, p.status, 807);
           if (!ok) break;
           tc_fence_after();
           const uint64_t dK_mn = sdesc_sw128(sK + ks * C::kTileBytes, C::kChunkBytes, 1024);
-          const uint32_t tA = tmem + C::kColS + 128 * (u & 1);
+          const uint32_t tA = tmem + C::kColDP + 128 * (u & 1);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             mma_ts(tmem + C::kColDQ, tA + 32 * (kk >> 1) + 8 * (kk & 1), dK_mn + kk * (2048 >> 4),
@@ -271,10 +254,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           mma_commit(&dq_done[ks]);
         }
       }
-      // each issuer's MMAs are complete once its drain barrier flips; B's last
-      // dQ follows every MMA of A (it waited for the last dP through
-      // ds_ready), so `drain` alone tells the math that all are done
-      uint64_t* my_drain = issuer_a ? &drain_a : &drain;
+      // each issuer's MMAs are complete once its drain barrier flips; the last
+      // dQ follows every S and dP (the math waited for both before its dS), so
+      // `drain` alone tells the math that all are done
+      uint64_t* my_drain = role == 0 ? &drain_s : role == 1 ? &drain_p : &drain;
       mma_commit(my_drain);
       mbar_drain(my_drain, 0);
     }
@@ -296,9 +279,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     int u = 0;
     bool ok = true;
     for (int j = jfirst; j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
-      const int x = u & 1;
-      const uint32_t tS = tmem + C::kColS + 128 * x + lane_off + col0;
-      ok = mbar_wait_warp(&s_full[x], (u >> 1) & 1, &abort_flag, p.status, 901);
+      const int x = u & 1;  // dP buffer
+      const uint32_t tS = tmem + C::kColS + lane_off + col0;
+      const uint32_t tP = tmem + C::kColDP + 128 * x + lane_off + col0;
+      ok = mbar_wait_warp(&s_full, u & 1, &abort_flag, p.status, 901);
       if (!ok) break;
       tc_fence_after();
       // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
@@ -319,20 +303,22 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           pf[16 * h + e + 1] = ex2(t.y);
         }
       }
+      // S_u has been read: S_{u+1} may overwrite it
+      tc_fence_before();
+      mbar_arrive_warp(&s_free);
       if (partial) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           if (e >= lim) pf[e] = 0.f;
       }
-      ok = mbar_wait_warp(&dp_full[u % C::kVStages], (u / C::kVStages) & 1, &abort_flag, p.status,
-                          902);
+      ok = mbar_wait_warp(&dp_full[x], (u >> 1) & 1, &abort_flag, p.status, 902);
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[16];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         uint32_t rp[16];
-        FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + col0 + 16 * h, rp);
+        FA_TMEM_LD16_SYNC(tP + 16 * h, rp);
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])), nd2);
@@ -340,9 +326,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
         }
       }
-      // packed dS of keys [col0, col0 + 32) over S columns [col0, col0 + 16),
+      // packed dS of keys [col0, col0 + 32) over dP columns [col0, col0 + 16),
       // which this thread has read
-      FA_TMEM_ST16(tS, dsp);
+      FA_TMEM_ST16(tP, dsp);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&ds_ready[x]);
