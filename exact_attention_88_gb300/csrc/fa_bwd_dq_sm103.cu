@@ -292,10 +292,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       if (p.causal) lim = min(lim, q - key0 + 1);
       const bool partial = lim < 32;
       float pf[32];
+      uint32_t rs_all[32];
+      FA_TMEM_LD32_SYNC(tS, rs_all);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t rs[16];
-        FA_TMEM_LD16_SYNC(tS + 16 * h, rs);
+        const uint32_t* rs = rs_all + 16 * h;
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const float2 t = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl22);
@@ -315,10 +316,11 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[16];
+      uint32_t rp_all[32];
+      FA_TMEM_LD32_SYNC(tP, rp_all);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t rp[16];
-        FA_TMEM_LD16_SYNC(tP + 16 * h, rp);
+        const uint32_t* rp = rp_all + 16 * h;
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])), nd2);

@@ -346,11 +346,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // P^T of half h goes over S^T columns [col0 + 8h, col0 + 8h + 8), which
       // were read in half 0
       float pf[32];
+      uint32_t rs_all[32];
+      FA_TMEM_LD32_SYNC(tmem + C::kColS + lane_off + col0, rs_all);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c0 = col0 + 16 * h;
-        uint32_t rs[16];
-        FA_TMEM_LD16_SYNC(tmem + C::kColS + lane_off + c0, rs);
+        const uint32_t* rs = rs_all + 16 * h;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const float4 L = *reinterpret_cast<const float4*>(&s_nl2[c0 + 4 * g]);
@@ -382,11 +383,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t dsp[16];
+      uint32_t rp_all[32];
+      FA_TMEM_LD32_SYNC(tmem + C::kColDP + lane_off + col0, rp_all);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c0 = col0 + 16 * h;
-        uint32_t rp[16];
-        FA_TMEM_LD16_SYNC(tmem + C::kColDP + lane_off + c0, rp);
+        const uint32_t* rp = rp_all + 16 * h;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const float4 Dd = *reinterpret_cast<const float4*>(&s_nD[c0 + 4 * g]);

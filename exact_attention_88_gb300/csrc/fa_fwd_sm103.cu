@@ -104,7 +104,7 @@ __device__ __forceinline__ float max64(const uint32_t* r) {
 
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
-                                             bool first, float& m, float& l) {
+                                             bool first, float& m, float& l, uint64_t* p_half) {
   // keys [0, lim) of the tile are visible from this row
   int lim = kv_limit - key0;
   if (causal) lim = min(lim, row - key0 + 1);
@@ -127,6 +127,18 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
     m = m_new;
   }
+  // O holds the sum up to the previous key tile (its P V is complete: this
+  // tile's S was issued after it); rescale when the running max moved -- before
+  // any of this tile's P is released to the tensor core
+  if (!first && __any_sync(0xffffffffu, grow)) {
+    for (int c = 0; c < ocols32; ++c) {
+      uint32_t o[32];
+      FA_TMEM_LD32_SYNC(tO + c * 32, o);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+      FA_TMEM_ST32(tO + c * 32, o);
+    }
+  }
   const float nm = (m == -INFINITY) ? 0.f : -m;
   const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
   float2 acc[8];
@@ -148,22 +160,18 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     // packed P of keys [64 half, 64 half + 64) over S columns [32 half, 32 half + 32),
     // which this thread has already read
     FA_TMEM_ST32(tS + 32 * half, pk);
+    if (half == 0) {
+      // keys [0, 64) of P are in place (and O rescaled): the first half of
+      // O += P V may start while the second half of P is computed
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(p_half);
+    }
   }
   const float2 s01 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
   const float2 s23 = add2(add2(acc[4], acc[5]), add2(acc[6], acc[7]));
   const float2 st = add2(s01, s23);
   l = l * alpha + (st.x + st.y);
-  // O holds the sum up to the previous key tile (its P V is complete: this
-  // tile's S was issued after it); rescale when the running max moved
-  if (!first && __any_sync(0xffffffffu, grow)) {
-    for (int c = 0; c < ocols32; ++c) {
-      uint32_t o[32];
-      FA_TMEM_LD32_SYNC(tO + c * 32, o);
-#pragma unroll
-      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-      FA_TMEM_ST32(tO + c * 32, o);
-    }
-  }
   tmem_wait_st();
 }
 
@@ -176,7 +184,7 @@ __global__ void __launch_bounds__(352, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t q_full, drain[2];
-  __shared__ uint64_t s_full[2], p_full[2], o_done[2], turn[2];  // per query tile
+  __shared__ uint64_t s_full[2], p_half[2], p_full[2], o_done[2], turn[2];  // per query tile
   // turn[x]: tile x's softmax may run.  The two softmax warpgroups take turns
   // key tile by key tile (A, B, A, B, ...), so that each runs alone on the
   // SMSPs while the tensor core works for the other tile.
@@ -209,7 +217,8 @@ __global__ void __launch_bounds__(352, 1)
     mbar_init(&drain[1], 1);
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 4);  // one arrival per softmax warp
+      mbar_init(&p_half[x], 4);  // one arrival per softmax warp: keys [0, 64) of P
+      mbar_init(&p_full[x], 4);  // all of P
       mbar_init(&turn[x], 4);
       mbar_init(&o_done[x], 1);
     }
@@ -314,14 +323,21 @@ __global__ void __launch_bounds__(352, 1)
         ok = mbar_wait(&v_full[st], ph, &abort_flag, p.status, 207);
         if (!ok) break;
         if (vis) {
-          // O_x += P_x V_j, P_x read from TMEM (packed, 8 columns per 16 keys)
+          // O_x += P_x V_j, P_x read from TMEM (packed, 8 columns per 16 keys):
+          // keys [0, 64) as soon as the softmax has written them, then the rest
+          const uint64_t dV = sdesc_sw128(sV + st * C::kTileBytes, C::kChunkBytes, 1024);
+          ok = mbar_wait(&p_half[x], cnt & 1, &abort_flag, p.status, 209 + x);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts(tO, tS + ks * 8, dV + ks * (2048 >> 4), idesc_pv, (cnt > 0 || ks > 0) ? 1u : 0u);
           ok = mbar_wait(&p_full[x], cnt & 1, &abort_flag, p.status, 205 + x);
           if (!ok) break;
           tc_fence_after();
-          const uint64_t dV = sdesc_sw128(sV + st * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tO, tS + ks * 8, dV + ks * (2048 >> 4), idesc_pv, (cnt > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 4; ks < 8; ++ks)
+            mma_ts(tO, tS + ks * 8, dV + ks * (2048 >> 4), idesc_pv, 1u);
           mma_commit(&o_done[x]);
           ++cnt;
         }
@@ -358,7 +374,7 @@ __global__ void __launch_bounds__(352, 1)
           if (!ok) break;
           tc_fence_after();
           softmax_tile(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0, p.scale_log2, n == 0,
-                       m, l);
+                       m, l, &p_half[x]);
           tc_fence_before();
           mbar_arrive_warp(&p_full[x]);
           ++n;
