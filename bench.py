@@ -147,6 +147,11 @@ def run_gpu(args, rank, world, local_rank):
 
     kernels = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
     ev = {n: [] for n in kernels}
+    # dK/dV and dQ read the same inputs and write disjoint outputs: in the timed
+    # steps dQ runs on a second stream, so either kernel's last CTAs overlap
+    # the other's; the per-kernel pass runs all four on one stream
+    stream2 = torch.cuda.Stream(dev)
+    ev_pre, ev_dq = torch.cuda.Event(), torch.cuda.Event()
 
     def step(record):
         def mark(name, fn):
@@ -160,10 +165,17 @@ def run_gpu(args, rank, world, local_rank):
                 fn()
         mark("fwd", lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, stream))
         mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
+        dq_stream = stream if record else stream2
+        if not record:
+            ev_pre.record(stream)
+            stream2.wait_event(ev_pre)
         mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv(q, k, v, do, lse, D, dk, dv, B, H, N, d, scale,
                                                 w.causal, mask, stream))
         mark("bwd_dq", lambda: fa.fa_bwd_dq(q, k, v, do, lse, D, dq, B, H, N, d, scale, w.causal,
-                                            mask, stream))
+                                            mask, dq_stream))
+        if not record:
+            ev_dq.record(stream2)
+            stream.wait_event(ev_dq)  # the next step's forward rewrites o and lse
 
     dist = None
     if world > 1:
@@ -271,7 +283,8 @@ def run_gpu(args, rank, world, local_rank):
 
 def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
     """Same metric through the public API with host buffers: pinned host inputs
-    copied in, fa_fwd + fa_bwd, results (O, lse, dQ, dK, dV) copied out, all
+    copied in, fa_fwd and the three backward steps (dQ on a second stream, as
+    in the device-resident steps), results (O, lse, dQ, dK, dV) copied out, all
     inside the timed region."""
     B, H, N, d = w.B, w.H, w.N, w.d
     host = {n: torch.from_numpy(case[n + "_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -285,15 +298,26 @@ def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
     g = {n: torch.empty_like(dev_in["q"]) for n in ("dq", "dk", "dv")}
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    D = ws[: B * H * N * 4].view(torch.float32)
     stream = torch.cuda.current_stream(dev)
+    stream2 = torch.cuda.Stream(dev)
+    ev_pre, ev_dq = torch.cuda.Event(), torch.cuda.Event()
 
     def step():
         for n in host:
             dev_in[n].copy_(host[n], non_blocking=True)
-        fa.fa_fwd(dev_in["q"], dev_in["k"], dev_in["v"], o, lse, B, H, N, d, w.scale, w.causal,
-                  mask, stream)
-        fa.fa_bwd(dev_in["q"], dev_in["k"], dev_in["v"], o, dev_in["do"], lse, g["dq"], g["dk"],
-                  g["dv"], ws, ws_bytes, B, H, N, d, w.scale, w.causal, mask, stream)
+        qd, kd, vd, dod = dev_in["q"], dev_in["k"], dev_in["v"], dev_in["do"]
+        fa.fa_fwd(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, mask, stream)
+        # the backward's three public steps, dQ beside dK/dV on a second stream
+        fa.fa_bwd_preprocess(o, dod, D, B, H, N, d, stream)
+        ev_pre.record(stream)
+        stream2.wait_event(ev_pre)
+        fa.fa_bwd_dkdv(qd, kd, vd, dod, lse, D, g["dk"], g["dv"], B, H, N, d, w.scale, w.causal,
+                       mask, stream)
+        fa.fa_bwd_dq(qd, kd, vd, dod, lse, D, g["dq"], B, H, N, d, w.scale, w.causal, mask,
+                     stream2)
+        ev_dq.record(stream2)
+        stream.wait_event(ev_dq)
         outs["o"].copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         for n in ("dq", "dk", "dv"):
