@@ -31,7 +31,7 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import WORKLOADS, generate, flops  # noqa: E402
+from workloads import WORKLOADS, generate, flops, sha256  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal, 1 GB300) and % of dense bf16 peak"
 DEFAULT_WORKLOAD = "long_causal_d128"
@@ -115,6 +115,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# replicas: every rank runs the whole workload on its own GPU; the job's time
+# is the slowest rank's, its work the sum over ranks
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(elapsed_ms, dist, device):
+    """Timed-region duration of the job: the max over ranks (dist = None: one rank)."""
+    if dist is None:
+        return elapsed_ms
+    import torch
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(step_flops, steps, elapsed_ms, world):
+    """TFLOP/s of the whole job: `world` replicas each did `steps` steps."""
+    return world * step_flops * steps / (elapsed_ms * 1e-3) / 1e12
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
 
@@ -135,6 +155,18 @@ def run_gpu(args, rank, world, local_rank):
     mask = fa.make_mask(kv_len, bmask)
     kept = kept_fraction(case["block_mask"])
     fwd_flops, step_flops = flops(w, kept)
+    # secondary FLOP figures, labelled: dense-equivalent for block-sparse (every
+    # tile counted), effective for key padding (sum_b N * kv_len[b] instead of
+    # B * N^2)
+    dense_step_flops = flops(w)[1]
+    eff_step_flops = None
+    if case["kv_len"] is not None:
+        eff_step_flops = step_flops * float(np.sum(np.minimum(case["kv_len"], N))) / (B * N)
+    inputs_sha256 = {n: sha256(case[n + "_bits"]) for n in ("q", "k", "v", "do")}
+    if case["kv_len"] is not None:
+        inputs_sha256["kv_len"] = sha256(case["kv_len"])
+    if case["block_mask"] is not None:
+        inputs_sha256["block_mask"] = sha256(case["block_mask"])
 
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -215,13 +247,9 @@ def run_gpu(args, rank, world, local_rank):
         raise RuntimeError("device status %d at site %d in the timed region" % (code, site))
     per_kernel = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in kernels}
 
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = whole_job_tflops(step_flops, args.steps, elapsed_ms, world)
     if rank != 0:
         return None
     peaks, peak_kind = measured_peaks()
@@ -255,6 +283,7 @@ def run_gpu(args, rank, world, local_rank):
                   (4 * q.numel() * 2 >> 20),
         },
         "pct_of_peak": round(100.0 * (value / world) / peak, 2),
+        "inputs_sha256": inputs_sha256,
         "kernels_ms": {n: round(t, 4) for n, t in per_kernel.items()},
         "roofline": {
             "kernel": "fa_bwd_dkdv (S^T, dP^T, dV, dK on tcgen05)",
@@ -276,6 +305,14 @@ def run_gpu(args, rank, world, local_rank):
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
+    if kept is not None:
+        result["dense_equivalent"] = {
+            "value": round(world * dense_step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "note": "every 128x128 tile counted, skipped ones included"}
+    if eff_step_flops is not None:
+        result["effective"] = {
+            "value": round(world * eff_step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "note": "sum_b N * kv_len[b] in place of B * N^2"}
     if not args.no_extras:
         result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args)
     return result
