@@ -169,3 +169,48 @@ def test_workload_sampled(fa, name):
     tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
     per = np.linalg.norm(dk64, axis=(2, 3))
     assert np.all(tot <= 2e-2 * per)
+
+
+# ---------------------------------------------------------------------------
+# 64K-token causal contexts.  Query rows: 256 sampled per head (O, lse, dQ).
+# Key rows: the last key tile, exactly -- under the causal mask only the last
+# 128 query rows see those keys, so the oracle needs the statistics (lse, D)
+# of those rows only.
+# ---------------------------------------------------------------------------
+
+@pytest.mark.slow
+@pytest.mark.parametrize("d", [128, 64])
+def test_causal_64k(fa, d):
+    B, H, N = 1, 2, 65536
+    case = random_case(B, H, N, d, seed=21 + d, value_scale=0.5)
+    scale = d ** -0.5
+    t = to_device(case, "bf16")
+    o, lse, (dq, dk, dv) = run(fa, t, scale, True)
+    to, tl, tg = TOL["bf16"]
+    rng = np.random.default_rng(64)
+    rows = np.stack([np.stack([np.sort(np.concatenate(
+        [[0, 127, 128, N - 1], rng.choice(np.arange(129, N - 1), 252, replace=False)]))
+        for _ in range(H)]) for _ in range(B)])
+    take = lambda a, r: np.take_along_axis(a, r[..., None], axis=2)
+    ro, rl = oracle.forward_rows(case["q"], case["k"], case["v"], scale, rows, causal=True)
+    assert max_abs(take(f64(o), rows), ro) <= to
+    assert max_abs(np.take_along_axis(lse.cpu().numpy().astype(np.float64), rows, axis=2),
+                   rl) <= tl
+    rdq = oracle.backward_query_rows(case["q"], case["k"], case["v"], case["do"], scale, rows,
+                                     causal=True)
+    assert rel_fro(take(f64(dq), rows), rdq) <= tg
+    last = np.broadcast_to(np.arange(N - 128, N), (B, H, 128)).copy()
+    lo, ll = oracle.forward_rows(case["q"], case["k"], case["v"], scale, last, causal=True)
+    lse_all = np.zeros((B, H, N))
+    d_all = np.zeros((B, H, N))
+    lse_all[..., N - 128:] = ll
+    d_all[..., N - 128:] = np.sum(np.asarray(case["do"][..., N - 128:, :], np.float64) * lo, -1)
+    rdk, rdv = oracle.backward_key_rows(case["q"], case["k"], case["v"], case["do"], scale, last,
+                                        lse_all, d_all, causal=True)
+    assert rel_fro(f64(dk)[..., N - 128:, :], rdk) <= tg
+    assert rel_fro(f64(dv)[..., N - 128:, :], rdv) <= tg
+    # any size: the key gradients of each head sum to zero
+    dk64 = f64(dk)
+    tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
+    per = np.linalg.norm(dk64, axis=(2, 3))
+    assert np.all(tot <= 2e-2 * per)

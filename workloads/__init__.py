@@ -4,10 +4,11 @@ This module holds no attention arithmetic: it draws random tensors, rounds
 them to the storage precision, and draws masks and sample indices.  Both the
 oracle-side tests and the GPU-side tests/bench take their inputs from here.
 
-The five workloads stand in for the workloads of the FlashAttention paper
-(summary page "FlashAttention: Fast and Memory-Efficient Exact Attention with
+The workloads stand in for the workloads of the FlashAttention paper (summary
+page "FlashAttention: Fast and Memory-Efficient Exact Attention with
 IO-Awareness", section "Results": GPT-2 at sequence length 1K, BERT-large at
-512, long-context causal models, block-sparse attention on long sequences),
+512, long-context causal models up to 64K tokens, block-sparse attention on
+long sequences),
 whose datasets and weights are not available: only the shapes, masks and value
 distributions are reproduced.
 
@@ -67,6 +68,9 @@ WORKLOADS = {
     # block-sparse attention on long sequences
     "block_sparse": Workload("block_sparse", 2, 16, 16384, 64, "bf16", False, "block_sparse",
                              sampled=True),
+    # 64K-token causal context (the pages' longest dense sequences), head dim 128
+    "causal_64k_d128": Workload("causal_64k_d128", 1, 4, 65536, 128, "bf16", True, "none",
+                                value_scale=0.5, sampled=True),
 }
 
 
