@@ -319,61 +319,94 @@ def run_gpu(args, rank, world, local_rank):
 
 
 def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
-    """Same metric through the public API with host buffers: pinned host inputs
-    copied in, fa_fwd and the three backward steps (dQ on a second stream, as
-    in the device-resident steps), results (O, lse, dQ, dK, dV) copied out, all
-    inside the timed region."""
+    """Same metric through the public API with host buffers: every step copies
+    its inputs in from pinned host memory, runs fa_fwd and the three backward
+    steps (dQ on a second stream, as in the device-resident steps) and copies
+    its results (O, lse, dQ, dK, dV) out, all inside the timed region.  Steps
+    are pipelined over two sets of device buffers: step k+1's inputs go in on
+    one copy stream and step k-1's results come out on another while step k
+    computes."""
     B, H, N, d = w.B, w.H, w.N, w.d
-    host = {n: torch.from_numpy(case[n + "_bits"].view(np.int16)).view(torch.bfloat16).pin_memory()
-            for n in ("q", "k", "v", "do")}
-    outs = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16).pin_memory()
-            for n in ("o", "dq", "dk", "dv")}
-    lse_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-    dev_in = {n: torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev) for n in host}
-    o = torch.empty_like(dev_in["q"])
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    g = {n: torch.empty_like(dev_in["q"]) for n in ("dq", "dk", "dv")}
+    shape = (B, H, N, d)
+    host_in = {n: torch.from_numpy(case[n + "_bits"].view(np.int16)).view(torch.bfloat16)
+               .pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = [{n: torch.empty(shape, dtype=torch.bfloat16).pin_memory()
+                 for n in ("o", "dq", "dk", "dv")} for _ in range(2)]
+    for h in host_out:
+        h["lse"] = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dev_in = [{n: torch.empty(shape, dtype=torch.bfloat16, device=dev) for n in host_in}
+              for _ in range(2)]
+    dev_out = [{n: torch.empty(shape, dtype=torch.bfloat16, device=dev)
+                for n in ("o", "dq", "dk", "dv")} for _ in range(2)]
+    for o in dev_out:
+        o["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     D = ws[: B * H * N * 4].view(torch.float32)
-    stream = torch.cuda.current_stream(dev)
-    stream2 = torch.cuda.Stream(dev)
+    s_comp = torch.cuda.current_stream(dev)
+    s_dq, s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_pre, ev_dq = torch.cuda.Event(), torch.cuda.Event()
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for n in host:
-            dev_in[n].copy_(host[n], non_blocking=True)
-        qd, kd, vd, dod = dev_in["q"], dev_in["k"], dev_in["v"], dev_in["do"]
-        fa.fa_fwd(qd, kd, vd, o, lse, B, H, N, d, w.scale, w.causal, mask, stream)
-        # the backward's three public steps, dQ beside dK/dV on a second stream
-        fa.fa_bwd_preprocess(o, dod, D, B, H, N, d, stream)
-        ev_pre.record(stream)
-        stream2.wait_event(ev_pre)
-        fa.fa_bwd_dkdv(qd, kd, vd, dod, lse, D, g["dk"], g["dv"], B, H, N, d, w.scale, w.causal,
-                       mask, stream)
-        fa.fa_bwd_dq(qd, kd, vd, dod, lse, D, g["dq"], B, H, N, d, w.scale, w.causal, mask,
-                     stream2)
-        ev_dq.record(stream2)
-        stream.wait_event(ev_dq)
-        outs["o"].copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        for n in ("dq", "dk", "dv"):
-            outs[n].copy_(g[n], non_blocking=True)
+    def copy_in(k):
+        x = dev_in[k % 2]
+        if k >= 2:
+            s_in.wait_event(comp_done[k % 2])  # step k-2 has read this set
+        with torch.cuda.stream(s_in):
+            for n in host_in:
+                x[n].copy_(host_in[n], non_blocking=True)
+        in_ready[k % 2].record(s_in)
 
-    for _ in range(args.warmup):
-        step()
+    def compute(k):
+        x, y = dev_in[k % 2], dev_out[k % 2]
+        s_comp.wait_event(in_ready[k % 2])
+        if k >= 2:
+            s_comp.wait_event(out_done[k % 2])  # step k-2's results have left this set
+        fa.fa_fwd(x["q"], x["k"], x["v"], y["o"], y["lse"], B, H, N, d, w.scale, w.causal, mask,
+                  s_comp)
+        fa.fa_bwd_preprocess(y["o"], x["do"], D, B, H, N, d, s_comp)
+        ev_pre.record(s_comp)
+        s_dq.wait_event(ev_pre)
+        fa.fa_bwd_dkdv(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dk"], y["dv"], B, H, N, d,
+                       w.scale, w.causal, mask, s_comp)
+        fa.fa_bwd_dq(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dq"], B, H, N, d, w.scale,
+                     w.causal, mask, s_dq)
+        ev_dq.record(s_dq)
+        s_comp.wait_event(ev_dq)
+        comp_done[k % 2].record(s_comp)
+
+    def copy_out(k):
+        y, h = dev_out[k % 2], host_out[k % 2]
+        s_out.wait_event(comp_done[k % 2])
+        with torch.cuda.stream(s_out):
+            for n in h:
+                h[n].copy_(y[n], non_blocking=True)
+        out_done[k % 2].record(s_out)
+
+    def run(n_steps):
+        copy_in(0)
+        for k in range(n_steps):
+            if k + 1 < n_steps:
+                copy_in(k + 1)
+            compute(k)
+            copy_out(k)
+
+    run(args.warmup)
     torch.cuda.synchronize(dev)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.steps):
-        step()
-    b.record(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(s_in)
+    run(args.steps)
+    s_out.wait_event(comp_done[(args.steps - 1) % 2])
+    t1.record(s_out)
     torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for t in outs.values()) + lse_h.numel() * 4
+    ms = t0.elapsed_time(t1) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0].values())
     return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipelined": "step k+1 copied in and step k-1 copied out while step k computes"}
 
 
 # ---------------------------------------------------------------------------
