@@ -4,7 +4,10 @@ Argument marshalling only: every step of the computation runs in the CUDA
 kernels of libfa.so.  The C functions keep their names (`fa_fwd`, `fa_bwd`,
 ...); each takes device pointers (ints or torch CUDA tensors) and raises
 `FaError` on a non-OK status.  `forward` / `backward` are conveniences that
-allocate the outputs with torch and call the same C functions.
+allocate the outputs with torch and call the same C functions; they accept
+[B, H, N, d] views of any layout whose last dimension is contiguous (for
+example a [B, N, H, d] buffer transposed to [B, H, N, d]) and pass each
+tensor's strides to the *_strided calls, so nothing is copied.
 
 Importing this package fails loudly if libfa.so has not been built
 (`python -c "import __graft_entry__ as g; g.build()"`): there is no fallback.
@@ -13,7 +16,9 @@ import ctypes
 import os
 
 __all__ = [
-    "FaError", "FaMask", "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
+    "FaError", "FaMask", "FaLayout", "FaLayouts", "layout_of", "make_layouts",
+    "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_fp32_strided", "fa_bwd_fp32_strided",
+    "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_fwd_fp32", "fa_bwd_fp32",
     "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
     "make_mask", "forward", "backward", "LIB_PATH",
@@ -41,6 +46,19 @@ class FaMask(ctypes.Structure):
                 ("block_mask", ctypes.c_void_p), ("block_size", ctypes.c_int)]
 
 
+class FaLayout(ctypes.Structure):
+    """Element strides of one [B, H, N, d] tensor (fa_layout)."""
+    _fields_ = [("batch", ctypes.c_int64), ("head", ctypes.c_int64), ("row", ctypes.c_int64)]
+
+
+_LAYOUT_NAMES = ("q", "k", "v", "o", "dO", "dq", "dk", "dv")
+
+
+class FaLayouts(ctypes.Structure):
+    """Layouts of the tensors of one call (fa_layouts)."""
+    _fields_ = [(n, FaLayout) for n in _LAYOUT_NAMES]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError("libfa.so is not built (expected at %s); run "
                       "__graft_entry__.build() first" % LIB_PATH)
@@ -51,6 +69,7 @@ _i = ctypes.c_int
 _f = ctypes.c_float
 _sz = ctypes.c_size_t
 _mp = ctypes.POINTER(FaMask)
+_lp = ctypes.POINTER(FaLayouts)
 
 _SIGS = {
     "fa_fwd": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _p],
@@ -67,6 +86,10 @@ _SIGS = {
     "fa_debug_wait_timeout": [ctypes.c_uint, _p],
     "fa_bwd_noalloc": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_last_cuda_error": [],
+    "fa_fwd_strided": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
+    "fa_fwd_fp32_strided": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
+    "fa_bwd_strided": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
+    "fa_bwd_fp32_strided": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -109,6 +132,57 @@ def make_mask(kv_len=None, block_mask=None, block_size=128):
     if block_mask is not None:
         return ctypes.pointer(FaMask(FA_MASK_BLOCK_SPARSE, None, _ptr(block_mask), block_size))
     return None
+
+
+def layout_of(t):
+    """FaLayout of a 4-D [B, H, N, d] tensor whose last dimension is contiguous."""
+    if t.dim() != 4:
+        raise ValueError("expected a [B, H, N, d] tensor")
+    if t.stride(3) != 1 and t.shape[3] > 1:
+        raise ValueError("the d elements of a row must be contiguous (stride(3) == 1)")
+    return FaLayout(t.stride(0), t.stride(1), t.stride(2))
+
+
+def make_layouts(**tensors):
+    """A pointer to an FaLayouts holding layout_of(t) for each named tensor
+    (names: q, k, v, o, dO, dq, dk, dv); entries not given stay zero, which
+    the calls that read them reject."""
+    unknown = set(tensors) - set(_LAYOUT_NAMES)
+    if unknown:
+        raise ValueError("unknown tensor names: %s" % sorted(unknown))
+    ls = FaLayouts()
+    for name, t in tensors.items():
+        setattr(ls, name, layout_of(t))
+    return ctypes.pointer(ls)
+
+
+def fa_fwd_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, layouts=None,
+                   stream=None):
+    _check(lib.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                              int(causal), mask, layouts, _stream(stream)), "fa_fwd_strided")
+
+
+def fa_fwd_fp32_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, layouts=None,
+                        stream=None):
+    _check(lib.fa_fwd_fp32_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                   scale, int(causal), mask, layouts, _stream(stream)),
+           "fa_fwd_fp32_strided")
+
+
+def fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                   scale, causal, mask=None, layouts=None, stream=None):
+    _check(lib.fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                              _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, B, H, N, d,
+                              scale, int(causal), mask, layouts, _stream(stream)),
+           "fa_bwd_strided")
+
+
+def fa_bwd_fp32_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                        scale, causal, mask=None, layouts=None, stream=None):
+    _check(lib.fa_bwd_fp32_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                   workspace_bytes, B, H, N, d, scale, int(causal), mask, layouts,
+                                   _stream(stream)), "fa_bwd_fp32_strided")
 
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, stream=None):
@@ -193,37 +267,45 @@ def fa_debug_wait_timeout(limit_us, stream=None):
 # conveniences: allocate outputs with torch, call the C functions
 # ---------------------------------------------------------------------------
 
-def _shape(q):
+def _shape(q, *others):
     if q.dim() != 4:
         raise ValueError("expected [B, H, N, d]")
+    for t in others:
+        if t.shape != q.shape or t.dtype != q.dtype or t.device != q.device:
+            raise ValueError("every tensor must match q in shape, dtype and device")
     return tuple(int(x) for x in q.shape)
 
 
 def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None):
-    """(O, lse) for contiguous CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32)."""
+    """(O, lse) for CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32) of any layout
+    whose last dimension is contiguous; O takes q's layout where torch can
+    keep it (torch.empty_like)."""
     import torch
-    B, H, N, d = _shape(q)
+    B, H, N, d = _shape(q, k, v)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     mask = make_mask(kv_len, block_mask)
-    fn = fa_fwd if q.dtype == torch.bfloat16 else fa_fwd_fp32
-    fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, stream)
+    layouts = make_layouts(q=q, k=k, v=v, o=o)
+    fn = fa_fwd_strided if q.dtype == torch.bfloat16 else fa_fwd_fp32_strided
+    fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, stream)
     return o, lse
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_mask=None,
              stream=None, workspace=None):
-    """(dQ, dK, dV) for the forward above and output gradient do."""
+    """(dQ, dK, dV) for the forward above and output gradient do; each
+    gradient takes the layout of its input where torch can keep it."""
     import torch
-    B, H, N, d = _shape(q)
+    B, H, N, d = _shape(q, k, v, o, do)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     mask = make_mask(kv_len, block_mask)
-    fn = fa_bwd if q.dtype == torch.bfloat16 else fa_bwd_fp32
+    layouts = make_layouts(q=q, k=k, v=v, o=o, dO=do, dq=dq, dk=dk, dv=dv)
+    fn = fa_bwd_strided if q.dtype == torch.bfloat16 else fa_bwd_fp32_strided
     fn(q, k, v, o, do, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, mask,
-       stream)
+       layouts, stream)
     return dq, dk, dv

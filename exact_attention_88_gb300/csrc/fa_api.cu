@@ -72,16 +72,41 @@ fa_status check_mask(const fa_mask* m, int* kind, const int32_t** kv, const uint
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Validates the caller's layout of one [B,H,N,d] tensor of `esize`-byte
+// elements (NULL: dense) and returns it with the stride of every size-1
+// dimension replaced by d, a value the TMA descriptor accepts and no index
+// ever multiplies by anything but 0.
+fa_status check_layout(const fa_layout* in, int B, int H, int N, int d, int esize, Layout* out) {
+  const Layout dl = dense_layout(H, N, d);
+  const long long given[3] = {in ? (long long)in->batch : dl.b, in ? (long long)in->head : dl.h,
+                              in ? (long long)in->row : dl.n};
+  const int extent[3] = {B, H, N};
+  long long r[3];
+  for (int i = 0; i < 3; ++i) {
+    if (extent[i] == 1) {
+      r[i] = d;
+      continue;
+    }
+    if (given[i] <= 0 || given[i] >= (1ll << 40) / esize) return FA_ERR_UNSUPPORTED;
+    if ((given[i] * esize) % 16 != 0) return FA_ERR_ALIGNMENT;
+    r[i] = given[i];
+  }
+  if (N > 1 && r[2] < d) return FA_ERR_UNSUPPORTED;
+  *out = Layout{r[0], r[1], r[2]};
+  return FA_OK;
+}
+
 }  // namespace
 
-bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
+bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B, int H, int N,
+                     int d, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)l.n * 2, (cuuint64_t)l.h * 2, (cuuint64_t)l.b * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -115,9 +140,14 @@ static bool attach_status(Args* a) {
 
 static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* v, void* o,
                           float* lse, int B, int H, int N, int d, float scale, int causal,
-                          const fa_mask* mask) {
+                          const fa_mask* mask, const fa_layouts* L, int esize) {
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  if ((st = check_layout(L ? &L->q : nullptr, B, H, N, d, esize, &a->lq)) != FA_OK ||
+      (st = check_layout(L ? &L->k : nullptr, B, H, N, d, esize, &a->lk)) != FA_OK ||
+      (st = check_layout(L ? &L->v : nullptr, B, H, N, d, esize, &a->lv)) != FA_OK ||
+      (st = check_layout(L ? &L->o : nullptr, B, H, N, d, esize, &a->lo)) != FA_OK)
+    return st;
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
@@ -133,9 +163,16 @@ static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* 
 }
 
 static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float scale, int causal,
-                                 const fa_mask* mask) {
+                                 const fa_mask* mask, const fa_layouts* L = nullptr,
+                                 int esize = 2) {
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  const fa_layout* in[8] = {L ? &L->q : nullptr,  L ? &L->k : nullptr,  L ? &L->v : nullptr,
+                            L ? &L->o : nullptr,  L ? &L->dO : nullptr, L ? &L->dq : nullptr,
+                            L ? &L->dk : nullptr, L ? &L->dv : nullptr};
+  Layout* out[8] = {&a->lq, &a->lk, &a->lv, &a->lo, &a->ldo, &a->ldq, &a->ldk, &a->ldv};
+  for (int t = 0; t < 8; ++t)
+    if ((st = check_layout(in[t], B, H, N, d, esize, out[t])) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   st = check_mask(mask, &a->mask_kind, &a->kv_len, &a->block_mask);
@@ -152,6 +189,25 @@ static fa_status split_workspace(BwdArgs* a, void* ws, size_t ws_bytes) {
   if (ws_bytes < round256((size_t)a->B * a->H * a->N * sizeof(float))) return FA_ERR_WORKSPACE;
   a->D = static_cast<float*>(ws);
   return FA_OK;
+}
+
+// Validation shared by the whole-backward calls (bf16: esize 2, fp32: 4).
+static fa_status fill_bwd_full(BwdArgs* a, const void* q, const void* k, const void* v,
+                               const void* o, const void* dO, const float* lse, void* dq,
+                               void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                               int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                               const fa_layouts* layouts, int esize) {
+  fa_status st = fill_bwd_common(a, B, H, N, d, scale, causal, mask, layouts, esize);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  st = split_workspace(a, workspace, workspace_bytes);
+  if (st != FA_OK) return st;
+  a->q = q; a->k = k; a->v = v; a->o = o; a->dO = dO; a->lse = lse;
+  a->dq = dq; a->dk = dk; a->dv = dv;
+  return attach_status(a) ? FA_OK : FA_ERR_CUDA;
 }
 
 // Text of the last CUDA error a call of this thread failed with.
@@ -185,8 +241,14 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, const fa_mask* mask, void* stream) {
+  return fa_fwd_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_layouts* layouts, void* stream) {
   FwdArgs a{};
-  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, 2);
   if (st != FA_OK) return st;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
@@ -195,8 +257,14 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                       int H, int N, int d, float scale, int causal, const fa_mask* mask,
                       void* stream) {
+  return fa_fwd_fp32_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
+}
+
+fa_status fa_fwd_fp32_strided(const float* q, const float* k, const float* v, float* o, float* lse,
+                              int B, int H, int N, int d, float scale, int causal,
+                              const fa_mask* mask, const fa_layouts* layouts, void* stream) {
   FwdArgs a{};
-  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, 4);
   if (st != FA_OK) return st;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_fwd_fp32(a, static_cast<cudaStream_t>(stream)));
@@ -206,23 +274,24 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                  const fa_mask* mask, void* stream) {
+  return fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                        scale, causal, mask, nullptr, stream);
+}
+
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                         float scale, int causal, const fa_mask* mask, const fa_layouts* layouts,
+                         void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_bwd_full(&a, q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B,
+                               H, N, d, scale, causal, mask, layouts, 2);
   if (st != FA_OK) return st;
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_ALIGNMENT;
-  st = split_workspace(&a, workspace, workspace_bytes);
-  if (st != FA_OK) return st;
-  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
-  a.dq = dq; a.dk = dk; a.dv = dv;
-  if (!attach_status(&a)) return FA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  fa_status st2 = launched(launch_bwd_preprocess(a, s));
-  if (st2 == FA_OK) st2 = launched(launch_bwd_dkdv_bf16(a, s));
-  if (st2 == FA_OK) st2 = launched(launch_bwd_dq_bf16(a, s));
-  return st2;
+  st = launched(launch_bwd_preprocess(a, s));
+  if (st == FA_OK) st = launched(launch_bwd_dkdv_bf16(a, s));
+  if (st == FA_OK) st = launched(launch_bwd_dq_bf16(a, s));
+  return st;
 }
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
@@ -273,18 +342,19 @@ fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const floa
                       const float* dO, const float* lse, float* dq, float* dk, float* dv,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                       float scale, int causal, const fa_mask* mask, void* stream) {
+  return fa_bwd_fp32_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N,
+                             d, scale, causal, mask, nullptr, stream);
+}
+
+fa_status fa_bwd_fp32_strided(const float* q, const float* k, const float* v, const float* o,
+                              const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                              float scale, int causal, const fa_mask* mask,
+                              const fa_layouts* layouts, void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_bwd_full(&a, q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B,
+                               H, N, d, scale, causal, mask, layouts, 4);
   if (st != FA_OK) return st;
-  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
-      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
-    return FA_ERR_ALIGNMENT;
-  st = split_workspace(&a, workspace, workspace_bytes);
-  if (st != FA_OK) return st;
-  a.q = q; a.k = k; a.v = v; a.o = o; a.dO = dO; a.lse = lse;
-  a.dq = dq; a.dk = dk; a.dv = dv;
-  if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_bwd_fp32(a, static_cast<cudaStream_t>(stream)));
 }
 

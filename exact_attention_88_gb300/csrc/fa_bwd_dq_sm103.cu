@@ -54,6 +54,7 @@ struct DqParams {
   const float* lse;
   const float* Dvec;
   __nv_bfloat16* dq;
+  Layout ldq;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   const int qi = p.T - 1 - lin / p.BH;  // causal: the last query tiles see the most keys: first
   const int bh = lin % p.BH;
   const int b = bh / p.H;
+  const int hd = bh - b * p.H;
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const int jkv = (kv_limit + 127) / 128;
@@ -144,15 +146,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       prefetch_tensormap(&tmDO);
       mbar_expect_tx(&q_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qi * 128, bh);
-        tma_load_3d(&tmDO, &q_full, smem + C::kOffDO + c * C::kChunkBytes, c * 64, qi * 128, bh);
+        tma_load_4d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qi * 128, hd, b);
+        tma_load_4d(&tmDO, &q_full, smem + C::kOffDO + c * C::kChunkBytes, c * 64, qi * 128, hd, b);
       }
       int jpf = jfirst, npf = 0;
       auto prefetch_upto = [&](int count) {
         for (; npf < count && jpf < ktiles.jend; ++npf, jpf = ktiles.next(jpf + 1))
           for (int c = 0; c < C::kChunks; ++c) {
-            tma_prefetch_3d(&tmK, c * 64, jpf * 128, bh);
-            tma_prefetch_3d(&tmV, c * 64, jpf * 128, bh);
+            tma_prefetch_4d(&tmK, c * 64, jpf * 128, hd, b);
+            tma_prefetch_4d(&tmV, c * 64, jpf * 128, hd, b);
           }
       };
       prefetch_upto(C::kPrefetchTiles);
@@ -165,15 +167,15 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
           break;
         mbar_expect_tx(&k_full[ks], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmK, &k_full[ks], smem + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, j * 128, bh);
+          tma_load_4d(&tmK, &k_full[ks], smem + C::kOffK + ks * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, hd, b);
         ++kcount[ks];
         if (!mbar_wait(&dp_full[vs], ((u / C::kVStages) & 1) ^ 1, &abort_flag, p.status, 702))
           break;
         mbar_expect_tx(&v_full[vs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmV, &v_full[vs], smem + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, j * 128, bh);
+          tma_load_4d(&tmV, &v_full[vs], smem + C::kOffV + vs * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, hd, b);
         ++vcount[vs];
       }
       // every issued copy must have landed before the CTA may exit
@@ -355,7 +357,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int e = 0; e < C::kDSlice; ++e) r[e] = 0u;  // no visible key: dQ = 0
       }
       if (q < p.N) {
-        uint4* dst = reinterpret_cast<uint4*>(p.dq + ((size_t)bh * p.N + q) * D + wg * C::kDSlice);
+        uint4* dst = reinterpret_cast<uint4*>(p.dq + row_offset(p.ldq, b, hd, q) + wg * C::kDSlice);
 #pragma unroll
         for (int g = 0; g < C::kDSlice / 8; ++g) {
           uint4 w;
@@ -383,13 +385,16 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   using C = DqCfg<D>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
-      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128))
+  if (!encode_bhnd_map(&mq, a.q, a.lq, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mk, a.k, a.lk, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mv, a.v, a.lv, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mdo, a.dO, a.ldo, a.B, a.H, a.N, D, 128))
     return cudaErrorInvalidValue;
   DqParams p;
   p.lse = a.lse;
   p.Dvec = a.D;
   p.dq = static_cast<__nv_bfloat16*>(a.dq);
+  p.ldq = a.ldq;
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
   p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
   p.H = a.H;

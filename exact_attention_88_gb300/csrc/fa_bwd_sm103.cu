@@ -62,6 +62,7 @@ struct BwdParams {
   const float* Dvec;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  Layout ldk, ldv;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int kt = lin / p.BH;  // key tile (causal: low tiles have the most work: first)
   const int bh = lin % p.BH;
   const int b = bh / p.H;
+  const int hd = bh - b * p.H;
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const bool keys_live = kt * 128 < kv_limit;  // else every key of the tile is padding
@@ -162,8 +164,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       prefetch_tensormap(&tmDO);
       mbar_expect_tx(&kv_full, 2 * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, bh);
-        tma_load_3d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, bh);
+        tma_load_4d(&tmK, &kv_full, smem + C::kOffK + c * C::kChunkBytes, c * 64, kt * 128, hd, b);
+        tma_load_4d(&tmV, &kv_full, smem + C::kOffV + c * C::kChunkBytes, c * 64, kt * 128, hd, b);
       }
       int qcount[C::kQStages] = {}, dcount[C::kDOStages] = {};
       // L2 prefetch of the Q / dO tiles a few query tiles ahead of their loads,
@@ -172,8 +174,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       auto prefetch_upto = [&](int count) {
         for (; npf < count && ipf < iend; ++npf, ipf = qtiles.next(ipf + 1))
           for (int c = 0; c < C::kChunks; ++c) {
-            tma_prefetch_3d(&tmQ, c * 64, ipf * 128, bh);
-            tma_prefetch_3d(&tmDO, c * 64, ipf * 128, bh);
+            tma_prefetch_4d(&tmQ, c * 64, ipf * 128, hd, b);
+            tma_prefetch_4d(&tmDO, c * 64, ipf * 128, hd, b);
           }
       };
       prefetch_upto(C::kPrefetchTiles);
@@ -185,15 +187,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           break;
         mbar_expect_tx(&q_full[qs], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmQ, &q_full[qs], smem + C::kOffQ + qs * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, i * 128, bh);
+          tma_load_4d(&tmQ, &q_full[qs], smem + C::kOffQ + qs * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, i * 128, hd, b);
         ++qcount[qs];
         if (!mbar_wait(&do_empty[ds], ((it / C::kDOStages) & 1) ^ 1, &abort_flag, p.status, 402))
           break;
         mbar_expect_tx(&do_full[ds], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmDO, &do_full[ds],
-                      smem + C::kOffDO + ds * C::kTileBytes + c * C::kChunkBytes, c * 64, i * 128, bh);
+          tma_load_4d(&tmDO, &do_full[ds],
+                      smem + C::kOffDO + ds * C::kTileBytes + c * C::kChunkBytes, c * 64, i * 128, hd,
+                      b);
         ++dcount[ds];
       }
       mbar_drain(&kv_full, 0);
@@ -425,7 +428,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const bool live = __all_sync(0xffffffffu, ok && !abort_flag);
     if (live) {
       tc_fence_after();
-      const size_t base = (head_row0 + key) * D + wg * C::kDSlice;
+      const long long base_v = row_offset(p.ldv, b, hd, key) + wg * C::kDSlice;
+      const long long base_k = row_offset(p.ldk, b, hd, key) + wg * C::kDSlice;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         uint32_t rr[C::kDSlice];
@@ -440,7 +444,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < C::kDSlice; ++e) rr[e] = 0u;
         }
-        if (key < p.N) store_row_bf16((which == 0 ? p.dv : p.dk) + base, rr, C::kDSlice);
+        if (key < p.N)
+          store_row_bf16(which == 0 ? p.dv + base_v : p.dk + base_k, rr, C::kDSlice);
       }
     }
   }
@@ -459,14 +464,18 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   using C = BwdCfg<D>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv, mdo;
-  if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
-      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128) || !encode_bhnd_map(&mdo, a.dO, BH, a.N, D, 128))
+  if (!encode_bhnd_map(&mq, a.q, a.lq, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mk, a.k, a.lk, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mv, a.v, a.lv, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mdo, a.dO, a.ldo, a.B, a.H, a.N, D, 128))
     return cudaErrorInvalidValue;
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.D;
   p.dk = static_cast<__nv_bfloat16*>(a.dk);
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
+  p.ldk = a.ldk;
+  p.ldv = a.ldv;
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
   p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
   p.H = a.H;

@@ -106,24 +106,27 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA: 3-D tiled bulk tensor load into shared memory, completion counted in
-// bytes on an mbarrier.  Coordinates are (x = column, y = row, z = head).
+// TMA: 4-D tiled bulk tensor load into shared memory, completion counted in
+// bytes on an mbarrier.  Coordinates are (x = column, y = row, h = head,
+// b = batch element); the tensor map carries the three strides, so any
+// layout whose d elements of a row are contiguous is read the same way.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_3d(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
-                                            int y, int z) {
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst, int x,
+                                            int y, int h, int b) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(h), "r"(b)
       : "memory");
 }
 
 // TMA: bring a tile of a tensor into L2 ahead of its load (no completion
 // signal; a hint that never faults on coordinates outside the tensor).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int h,
+                                                int b) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
+               "r"(x), "r"(y), "r"(h), "r"(b)
                : "memory");
 }
 
@@ -133,28 +136,6 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
 __device__ __forceinline__ void mbar_arrive_warp(uint64_t* bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
-// TMA: element-wise add of a shared-memory tile into global memory (fp32),
-// tracked by the issuing thread's bulk-async group.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* src, int x,
-                                                  int y, int z) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(x), "r"(y), "r"(z), "r"(smem_addr(src))
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// the source shared memory of every committed bulk op of this thread may be reused
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// every committed bulk op of this thread has completed
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
@@ -411,15 +392,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void red_add_f32(float* addr, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

@@ -35,6 +35,7 @@ struct F32Params {
   float* dq;
   float* dk;
   float* dv;
+  Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T;
@@ -62,12 +63,17 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const F32Params p) {
   const int bh = blockIdx.y, b = bh / p.H;
   const int part = threadIdx.x & 3;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 2);
-  const size_t head = (size_t)bh * p.N;
+  const size_t head = (size_t)bh * p.N;  // lse and D rows (dense)
+  const int hd = bh - b * p.H;
+  const float* qh = p.q + row_offset(p.lq, b, hd, 0);
+  const float* kh = p.k + row_offset(p.lk, b, hd, 0);
+  const float* vh = p.v + row_offset(p.lv, b, hd, 0);
+  float* ooh = p.out_o + row_offset(p.lo, b, hd, 0);
   const int kv_limit = p.kv_len ? max(0, min(p.kv_len[b], p.N)) : p.N;
   float qr[E], acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
-    qr[e] = row < p.N ? p.q[(head + row) * D + 4 * e + part] : 0.f;
+    qr[e] = row < p.N ? qh[(long long)row * p.lq.n + 4 * e + part] : 0.f;
     acc[e] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -75,8 +81,8 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const F32Params p) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kTileKeys * D; idx += blockDim.x) {
       const int jj = idx / D, c = idx % D, j = j0 + jj;
-      sK[jj][c] = j < p.N ? p.k[(head + j) * D + c] : 0.f;
-      sV[jj][c] = j < p.N ? p.v[(head + j) * D + c] : 0.f;
+      sK[jj][c] = j < p.N ? kh[(long long)j * p.lk.n + c] : 0.f;
+      sV[jj][c] = j < p.N ? vh[(long long)j * p.lv.n + c] : 0.f;
     }
     __syncthreads();
     float s[kTileKeys];
@@ -109,7 +115,7 @@ __global__ void __launch_bounds__(128) fwd_fp32_kernel(const F32Params p) {
     const bool empty = !(l > 0.f);
     const float inv = empty ? 0.f : 1.f / l;
 #pragma unroll
-    for (int e = 0; e < E; ++e) p.out_o[(head + row) * D + 4 * e + part] = acc[e] * inv;
+    for (int e = 0; e < E; ++e) ooh[(long long)row * p.lo.n + 4 * e + part] = acc[e] * inv;
     if (part == 0) p.out_lse[head + row] = empty ? -INFINITY : m + logf(l);
   }
 }
@@ -121,16 +127,23 @@ __global__ void __launch_bounds__(128) bwd_fp32_dq_kernel(const F32Params p) {
   const int bh = blockIdx.y, b = bh / p.H;
   const int part = threadIdx.x & 3;
   const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 2);
-  const size_t head = (size_t)bh * p.N;
+  const size_t head = (size_t)bh * p.N;  // lse and D rows (dense)
+  const int hd = bh - b * p.H;
+  const float* qh = p.q + row_offset(p.lq, b, hd, 0);
+  const float* kh = p.k + row_offset(p.lk, b, hd, 0);
+  const float* vh = p.v + row_offset(p.lv, b, hd, 0);
+  const float* oh = p.o + row_offset(p.lo, b, hd, 0);
+  const float* doh = p.dO + row_offset(p.ldo, b, hd, 0);
+  float* dqh = p.dq + row_offset(p.ldq, b, hd, 0);
   const int kv_limit = p.kv_len ? max(0, min(p.kv_len[b], p.N)) : p.N;
   float qr[E], dor[E], g[E];
   float dd = 0.f;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const bool in = row < p.N;
-    qr[e] = in ? p.q[(head + row) * D + 4 * e + part] : 0.f;
-    dor[e] = in ? p.dO[(head + row) * D + 4 * e + part] : 0.f;
-    dd = fmaf(dor[e], in ? p.o[(head + row) * D + 4 * e + part] : 0.f, dd);
+    qr[e] = in ? qh[(long long)row * p.lq.n + 4 * e + part] : 0.f;
+    dor[e] = in ? doh[(long long)row * p.ldo.n + 4 * e + part] : 0.f;
+    dd = fmaf(dor[e], in ? oh[(long long)row * p.lo.n + 4 * e + part] : 0.f, dd);
     g[e] = 0.f;
   }
   dd = quad_sum(dd);
@@ -140,8 +153,8 @@ __global__ void __launch_bounds__(128) bwd_fp32_dq_kernel(const F32Params p) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kTileKeys * D; idx += blockDim.x) {
       const int jj = idx / D, c = idx % D, j = j0 + jj;
-      sK[jj][c] = j < p.N ? p.k[(head + j) * D + c] : 0.f;
-      sV[jj][c] = j < p.N ? p.v[(head + j) * D + c] : 0.f;
+      sK[jj][c] = j < p.N ? kh[(long long)j * p.lk.n + c] : 0.f;
+      sV[jj][c] = j < p.N ? vh[(long long)j * p.lv.n + c] : 0.f;
     }
     __syncthreads();
 #pragma unroll 2
@@ -163,7 +176,7 @@ __global__ void __launch_bounds__(128) bwd_fp32_dq_kernel(const F32Params p) {
   }
   if (row < p.N) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) p.dq[(head + row) * D + 4 * e + part] = g[e] * p.scale;
+    for (int e = 0; e < E; ++e) dqh[(long long)row * p.ldq.n + 4 * e + part] = g[e] * p.scale;
   }
 }
 
@@ -174,22 +187,29 @@ __global__ void __launch_bounds__(128) bwd_fp32_dkdv_kernel(const F32Params p) {
   const int bh = blockIdx.y, b = bh / p.H;
   const int part = threadIdx.x & 3;
   const int key = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 2);
-  const size_t head = (size_t)bh * p.N;
+  const size_t head = (size_t)bh * p.N;  // lse and D rows (dense)
+  const int hd = bh - b * p.H;
+  const float* qh = p.q + row_offset(p.lq, b, hd, 0);
+  const float* kh = p.k + row_offset(p.lk, b, hd, 0);
+  const float* vh = p.v + row_offset(p.lv, b, hd, 0);
+  const float* doh = p.dO + row_offset(p.ldo, b, hd, 0);
+  float* dkh = p.dk + row_offset(p.ldk, b, hd, 0);
+  float* dvh = p.dv + row_offset(p.ldv, b, hd, 0);
   const int kv_limit = p.kv_len ? max(0, min(p.kv_len[b], p.N)) : p.N;
   float kr[E], vr[E], gk[E], gv[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const bool in = key < p.N;
-    kr[e] = in ? p.k[(head + key) * D + 4 * e + part] : 0.f;
-    vr[e] = in ? p.v[(head + key) * D + 4 * e + part] : 0.f;
+    kr[e] = in ? kh[(long long)key * p.lk.n + 4 * e + part] : 0.f;
+    vr[e] = in ? vh[(long long)key * p.lv.n + 4 * e + part] : 0.f;
     gk[e] = gv[e] = 0.f;
   }
   for (int i0 = 0; i0 < p.N; i0 += kTileKeys) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kTileKeys * D; idx += blockDim.x) {
       const int ii = idx / D, c = idx % D, i = i0 + ii;
-      sQ[ii][c] = i < p.N ? p.q[(head + i) * D + c] : 0.f;
-      sDO[ii][c] = i < p.N ? p.dO[(head + i) * D + c] : 0.f;
+      sQ[ii][c] = i < p.N ? qh[(long long)i * p.lq.n + c] : 0.f;
+      sDO[ii][c] = i < p.N ? doh[(long long)i * p.ldo.n + c] : 0.f;
     }
     if (threadIdx.x < kTileKeys) {
       const int i = i0 + threadIdx.x;
@@ -221,8 +241,8 @@ __global__ void __launch_bounds__(128) bwd_fp32_dkdv_kernel(const F32Params p) {
   if (key < p.N) {
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-      p.dk[(head + key) * D + 4 * e + part] = gk[e] * p.scale;
-      p.dv[(head + key) * D + 4 * e + part] = gv[e];
+      dkh[(long long)key * p.ldk.n + 4 * e + part] = gk[e] * p.scale;
+      dvh[(long long)key * p.ldv.n + 4 * e + part] = gv[e];
     }
   }
 }
@@ -249,6 +269,10 @@ cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s) {
   p.v = static_cast<const float*>(a.v);
   p.out_o = static_cast<float*>(a.o);
   p.out_lse = a.lse;
+  p.lq = a.lq;
+  p.lk = a.lk;
+  p.lv = a.lv;
+  p.lo = a.lo;
   dim3 grid(tiles_of(a.N, kRowsPerBlock), a.B * a.H);
   if (a.d == 64)
     fwd_fp32_kernel<64><<<grid, 128, 0, s>>>(p);
@@ -269,6 +293,14 @@ cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s) {
   p.dq = static_cast<float*>(a.dq);
   p.dk = static_cast<float*>(a.dk);
   p.dv = static_cast<float*>(a.dv);
+  p.lq = a.lq;
+  p.lk = a.lk;
+  p.lv = a.lv;
+  p.lo = a.lo;
+  p.ldo = a.ldo;
+  p.ldq = a.ldq;
+  p.ldk = a.ldk;
+  p.ldv = a.ldv;
   dim3 grid(tiles_of(a.N, kRowsPerBlock), a.B * a.H);
   if (a.d == 64) {
     bwd_fp32_dq_kernel<64><<<grid, 128, 0, s>>>(p);

@@ -51,6 +51,7 @@ struct FwdCfg {
 
 struct FwdParams {
   __nv_bfloat16* o;
+  Layout lo;
   float* lse;
   const int32_t* kv_len;
   const uint8_t* block_mask;
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(352, 1)
   const int pair = p.pairs - 1 - lin / p.BH;
   const int bh = lin % p.BH;
   const int b = bh / p.H;
+  const int hd = bh - b * p.H;
   const int qa = 2 * pair, qb = 2 * pair + 1;  // query tiles; qb may be past the end
   const bool has_b = qb < p.T;
 
@@ -245,10 +247,10 @@ __global__ void __launch_bounds__(352, 1)
       prefetch_tensormap(&tmV);
       mbar_expect_tx(&q_full, (has_b ? 2 : 1) * C::kTileBytes);
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qa * 128, bh);
+        tma_load_4d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qa * 128, hd, b);
         if (has_b)
-          tma_load_3d(&tmQ, &q_full, smem + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, c * 64,
-                      qb * 128, bh);
+          tma_load_4d(&tmQ, &q_full, smem + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, c * 64,
+                      qb * 128, hd, b);
       }
       int kcount[C::kStages] = {}, vcount[C::kStages] = {};
       int u = 0;
@@ -260,15 +262,15 @@ __global__ void __launch_bounds__(352, 1)
         if (!ok) break;
         mbar_expect_tx(&k_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmK, &k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, j * 128, bh);
+          tma_load_4d(&tmK, &k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, hd, b);
         ++kcount[st];
         ok = mbar_wait(&v_empty[st], ph ^ 1, &abort_flag, p.status, 102);
         if (!ok) break;
         mbar_expect_tx(&v_full[st], C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(&tmV, &v_full[st], smem + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, j * 128, bh);
+          tma_load_4d(&tmV, &v_full[st], smem + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes,
+                      c * 64, j * 128, hd, b);
         ++vcount[st];
       }
       // every issued copy must have landed before the CTA may exit
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(352, 1)
       if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
         const bool empty_row = !(l > 0.f);
         const float inv = empty_row ? 0.f : 1.f / l;
-        const size_t base = ((size_t)bh * p.N + row) * D;
+        const long long base = row_offset(p.lo, b, hd, row);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
@@ -436,11 +438,13 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   using C = FwdCfg<D>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv;
-  if (!encode_bhnd_map(&mq, a.q, BH, a.N, D, 128) || !encode_bhnd_map(&mk, a.k, BH, a.N, D, 128) ||
-      !encode_bhnd_map(&mv, a.v, BH, a.N, D, 128))
+  if (!encode_bhnd_map(&mq, a.q, a.lq, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mk, a.k, a.lk, a.B, a.H, a.N, D, 128) ||
+      !encode_bhnd_map(&mv, a.v, a.lv, a.B, a.H, a.N, D, 128))
     return cudaErrorInvalidValue;
   FwdParams p;
   p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.lo = a.lo;
   p.lse = a.lse;
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
   p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;

@@ -15,13 +15,37 @@ namespace fa {
 // Code the kernels write into status[0] when a wait gives up (FA_ERR_TIMEOUT).
 constexpr int kStatusTimeoutCode = 6;
 
+// Element strides of a [B, H, N, d] tensor whose d elements per row are
+// contiguous: element (b, h, n, c) of layout l sits at base + b*l.b + h*l.h +
+// n*l.n + c.
+struct Layout {
+  long long b, h, n;
+};
+
+inline Layout dense_layout(int H, int N, int d) {
+  return Layout{(long long)H * N * d, (long long)N * d, (long long)d};
+}
+
+// True when l addresses a [B, H, N, d] tensor exactly as the dense layout
+// does (the strides of size-1 dimensions never matter).
+inline bool is_dense(const Layout& l, int B, int H, int N, int d) {
+  return (B == 1 || l.b == (long long)H * N * d) && (H == 1 || l.h == (long long)N * d) &&
+         (N == 1 || l.n == d);
+}
+
+// Offset in elements of row n of head (b, h).
+__host__ __device__ inline long long row_offset(const Layout& l, int b, int h, int n) {
+  return (long long)b * l.b + (long long)h * l.h + (long long)n * l.n;
+}
+
 // Everything a forward launch needs.  Pointers are device pointers.
 struct FwdArgs {
   const void* q;
   const void* k;
   const void* v;
   void* o;
-  float* lse;
+  float* lse;  // dense fp32 [B,H,N]
+  Layout lq, lk, lv, lo;
   int B, H, N, d;
   float scale;
   int causal;
@@ -42,6 +66,7 @@ struct BwdArgs {
   void* dq;
   void* dk;
   void* dv;
+  Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
   int B, H, N, d;
   float scale;
   int causal;
@@ -51,10 +76,12 @@ struct BwdArgs {
   int* status;
 };
 
-// Encodes a 3-D TMA descriptor over a [BH, N, d] bf16 tensor: x = column
-// (d), y = row (N), z = head; box = 64 columns x box_rows rows x 1 head,
-// 128-byte swizzle, out-of-range rows read as zero.
-bool encode_bhnd_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+// Encodes a 4-D TMA descriptor over a [B, H, N, d] bf16 tensor with layout
+// l: x = column (d), y = row (N), then head and batch element; box = 64
+// columns x box_rows rows x 1 x 1, 128-byte swizzle, out-of-range rows read
+// as zero.
+bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B, int H, int N,
+                     int d, int box_rows);
 
 // Device address of the status block of the current device (no allocation:
 // it is a __device__ variable), or nullptr on failure.

@@ -54,8 +54,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (need > fa::kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;  // beyond the fixed scratch
   void* scratch = fa::scratch_address();
   if (!scratch) return FA_ERR_CUDA;
-  // fa_bwd validates every argument, writes D and zeroes the dQ accumulator in
-  // the scratch before using it, then runs the backward kernels on `stream`.
+  // fa_bwd validates every argument and writes D into the scratch before any
+  // kernel reads it, then runs the backward kernels on `stream`.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, scratch, fa::kNoAllocScratchBytes, B, H, N, d,
                 scale, causal, mask, stream);
 }

@@ -48,8 +48,8 @@ __global__ void __launch_bounds__(128, 1)
       uint32_t bytes = (uint32_t)N * K * 2 + (a_tmem ? 0u : (uint32_t)kProbeM * K * 2);
       mbar_expect_tx(&bar_load, bytes);
       for (int c = 0; c < kchunks; ++c) {
-        if (!a_tmem) tma_load_3d(&tmA, &bar_load, sA + c * kProbeM * 128, c * 64, 0, 0);
-        tma_load_3d(&tmB, &bar_load, sB + c * N * 128, c * 64, 0, 0);
+        if (!a_tmem) tma_load_4d(&tmA, &bar_load, sA + c * kProbeM * 128, c * 64, 0, 0, 0);
+        tma_load_4d(&tmB, &bar_load, sB + c * N * 128, c * 64, 0, 0, 0);
       }
     }
   } else {
@@ -163,8 +163,9 @@ cudaError_t launch_umma_probe(const void* a, const void* b, float* d, int M, int
   (void)M;
   CUtensorMap ma{}, mb{};
   if (use_tma) {
-    if (!encode_bhnd_map(&ma, a, 1, kProbeM, K, kProbeM)) return cudaErrorInvalidValue;
-    if (!encode_bhnd_map(&mb, b, 1, N, K, N)) return cudaErrorInvalidValue;
+    if (!encode_bhnd_map(&ma, a, dense_layout(1, kProbeM, K), 1, 1, kProbeM, K, kProbeM))
+      return cudaErrorInvalidValue;
+    if (!encode_bhnd_map(&mb, b, dense_layout(1, N, K), 1, 1, N, K, N)) return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(umma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kProbeSmem);

@@ -20,7 +20,9 @@
  *
  * Conventions shared by every call:
  *   - Tensors are dense row-major [B, H, N, d] (d contiguous) in DEVICE
- *     memory, 16-byte aligned; lse and D are fp32 [B, H, N].  The caller owns
+ *     memory, 16-byte aligned; lse and D are fp32 [B, H, N].  The *_strided
+ *     calls take Q, K, V, O, dO, dQ, dK, dV in any layout whose d elements of
+ *     a row are contiguous (fa_layout); lse and D stay dense.  The caller owns
  *     every buffer; the library allocates nothing.
  *   - bf16 calls take bf16 (uint16 storage) Q, K, V, O, dO, dQ, dK, dV and
  *     accumulate in fp32.  *_fp32 calls take fp32 everywhere.
@@ -131,6 +133,50 @@ fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const floa
                       const float* dO, const float* lse, float* dq, float* dk, float* dv,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                       float scale, int causal, const fa_mask* mask, void* stream);
+
+/* Layout of one [B, H, N, d] tensor as element strides: element (b, h, n, c)
+ * is at base + b*batch + h*head + n*row + c (the d elements of a row are
+ * contiguous).  Dense [B,H,N,d] is {H*N*d, N*d, d}; a [B,N,H,d] buffer (the
+ * heads of a packed projection side by side in each row) read as [B,H,N,d]
+ * is {N*H*d, d, H*d}.  Rules, checked on the host before any launch:
+ *   - the stride of a dimension of size 1 is ignored;
+ *   - every other stride is positive (FA_ERR_UNSUPPORTED otherwise), a
+ *     multiple of 16 bytes (8 bf16 or 4 fp32 elements; FA_ERR_ALIGNMENT
+ *     otherwise) and below 2^40 bytes (FA_ERR_UNSUPPORTED otherwise);
+ *   - the row stride is at least d when N > 1 (FA_ERR_UNSUPPORTED).
+ * An output must not overlap another tensor of the same call; this is not
+ * checked. */
+typedef struct {
+  int64_t batch, head, row;
+} fa_layout;
+
+/* Layouts of the tensors of one call.  The forward reads q, k, v, o and
+ * ignores the rest. */
+typedef struct {
+  fa_layout q, k, v, o, dO, dq, dk, dv;
+} fa_layouts;
+
+/* fa_fwd / fa_bwd / fa_fwd_fp32 / fa_bwd_fp32 with a layout per tensor
+ * (NULL = every tensor dense); every other argument as in the dense call.
+ * The work and the results are those of the dense call on the same values:
+ * the kernels read and write through the strides (the TMA descriptors of the
+ * bf16 kernels carry them), nothing is copied. */
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_layouts* layouts, void* stream);
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                         float scale, int causal, const fa_mask* mask, const fa_layouts* layouts,
+                         void* stream);
+fa_status fa_fwd_fp32_strided(const float* q, const float* k, const float* v, float* o, float* lse,
+                              int B, int H, int N, int d, float scale, int causal,
+                              const fa_mask* mask, const fa_layouts* layouts, void* stream);
+fa_status fa_bwd_fp32_strided(const float* q, const float* k, const float* v, const float* o,
+                              const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                              void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                              float scale, int causal, const fa_mask* mask,
+                              const fa_layouts* layouts, void* stream);
 
 /* Size of the fixed scratch array fa_bwd_noalloc works in: 32 MiB. */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -41,7 +41,8 @@ def f64(x):
 
 
 def max_abs(a, b, finite_only=False):
-    d = np.abs(a - b)
+    with np.errstate(invalid="ignore"):   # -inf - -inf where both rows are empty
+        d = np.abs(a - b)
     if finite_only:
         both_inf = np.isneginf(a) & np.isneginf(b)
         d = np.where(both_inf, 0.0, d)

@@ -134,3 +134,65 @@ def test_substeps_reject_bad_arguments(fa):
     assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 1, 0, 1, 0, None) == 1
     assert fa.lib.fa_debug_wait_timeout(0, None) == 1
     assert fa.lib.fa_debug_wait_timeout(2000000, None) == 1
+
+
+def strided(fa, fp32=False, bwd=False, B=2, H=2, N=128, d=64, **lay):
+    """Calls a *_strided entry point with fake pointers; `lay` overrides the
+    (batch, head, row) strides of named tensors, the rest dense."""
+    ls = fa.FaLayouts()
+    for name in ("q", "k", "v", "o", "dO", "dq", "dk", "dv"):
+        setattr(ls, name, fa.FaLayout(*lay.get(name, (H * N * d, N * d, d))))
+    L = ctypes.pointer(ls)
+    if not bwd:
+        fn = fa.lib.fa_fwd_fp32_strided if fp32 else fa.lib.fa_fwd_strided
+        return fn(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, N, d, 0.125, 0, None, L, None)
+    fn = fa.lib.fa_bwd_fp32_strided if fp32 else fa.lib.fa_bwd_strided
+    ws = fa.fa_bwd_workspace_size(B, H, N, d)
+    return fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, B, H, N, d, 0.125, 0,
+              None, L, None)
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+@pytest.mark.parametrize("fp32", [False, True])
+def test_strided_layout_rules(fa, fp32, bwd):
+    B, H, N, d = 2, 2, 128, 64
+    name = "dv" if bwd else "o"
+    # valid layouts pass validation and reach the CUDA runtime (absent here)
+    assert strided(fa, fp32, bwd) == 5
+    assert strided(fa, fp32, bwd, q=(N * H * d, d, H * d)) == 5          # [B,N,H,d]
+    assert strided(fa, fp32, bwd, **{name: (N * 3 * H * d, d, 3 * H * d)}) == 5  # packed QKV
+    # a zero, negative or overlapping stride is not supported
+    assert strided(fa, fp32, bwd, k=(H * N * d, 0, d)) == 2
+    assert strided(fa, fp32, bwd, v=(-H * N * d, N * d, d)) == 2
+    assert strided(fa, fp32, bwd, **{name: (H * N * d, N * d, d - 8)}) == 2
+    assert strided(fa, fp32, bwd, q=(1 << 40, N * d, d)) == 2
+    # strides must be multiples of 16 bytes
+    assert strided(fa, fp32, bwd, q=(H * N * d, N * d + 2, d)) == 3
+    assert strided(fa, fp32, bwd, **{name: (H * N * d + 4, N * d, d)}) == (5 if fp32 else 3)
+    # the strides of size-1 dimensions are ignored
+    assert strided(fa, fp32, bwd, B=1, q=(0, N * d, d), k=(-5, N * d, d)) == 5
+    assert strided(fa, fp32, bwd, H=1, N=1, q=(N * d, 3, 7)) == 5
+
+
+def test_strided_backward_needs_every_layout(fa):
+    # the forward ignores dO, dq, dk, dv; the backward rejects them when unset
+    ls = fa.FaLayouts()
+    for name in ("q", "k", "v", "o"):
+        setattr(ls, name, fa.FaLayout(2 * 128 * 64, 128 * 64, 64))
+    L = ctypes.pointer(ls)
+    assert fa.lib.fa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 0.125, 0, None, L,
+                                 None) == 5
+    ws = fa.fa_bwd_workspace_size(2, 2, 128, 64)
+    assert fa.lib.fa_bwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 2,
+                                 2, 128, 64, 0.125, 0, None, L, None) == 2
+
+
+def test_layout_of_reads_torch_strides(fa):
+    import torch
+    x = torch.zeros(2, 5, 3, 64).transpose(1, 2)   # [B,N,H,d] buffer seen as [B,H,N,d]
+    lo = fa.layout_of(x)
+    assert (lo.batch, lo.head, lo.row) == (5 * 3 * 64, 64, 3 * 64)
+    with pytest.raises(ValueError):
+        fa.layout_of(torch.zeros(2, 3, 64, 5).transpose(2, 3))   # d not contiguous
+    with pytest.raises(ValueError):
+        fa.make_layouts(x=x)
