@@ -46,7 +46,11 @@ fa_status check_sizes(int B, int H, int N, int d) {
   return FA_OK;
 }
 
-fa_status check_mask(const fa_mask* m, int* kind, const int32_t** kv, const uint8_t** bm) {
+// Tiles of one block-mask row the kernels can hold as a shared-memory bitmap.
+constexpr int kMaxMaskTiles = 4096;
+
+fa_status check_mask(const fa_mask* m, int N, int* kind, const int32_t** kv,
+                     const uint8_t** bm) {
   *kind = FA_MASK_NONE;
   *kv = nullptr;
   *bm = nullptr;
@@ -62,6 +66,7 @@ fa_status check_mask(const fa_mask* m, int* kind, const int32_t** kv, const uint
     case FA_MASK_BLOCK_SPARSE:
       if (!m->block_mask) return FA_ERR_INVALID_ARG;
       if (m->block_size != 128) return FA_ERR_UNSUPPORTED;
+      if (tiles_of(N, 128) > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
       *kind = FA_MASK_BLOCK_SPARSE;
       *bm = m->block_mask;
       return FA_OK;
@@ -153,7 +158,7 @@ static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* 
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  st = check_mask(mask, &a->mask_kind, &a->kv_len, &a->block_mask);
+  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask);
   if (st != FA_OK) return st;
   a->q = q; a->k = k; a->v = v; a->o = o; a->lse = lse;
   a->B = B; a->H = H; a->N = N; a->d = d;
@@ -175,7 +180,7 @@ static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float s
     if ((st = check_layout(in[t], B, H, N, d, esize, out[t])) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
-  st = check_mask(mask, &a->mask_kind, &a->kv_len, &a->block_mask);
+  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask);
   if (st != FA_OK) return st;
   a->B = B; a->H = H; a->N = N; a->d = d;
   a->scale = scale;

@@ -64,15 +64,12 @@ struct DqParams {
 };
 
 // Key tiles j that query tile qi sees: j < jend (causal diagonal, key
-// padding, end of sequence), block-mask row qi.
+// padding, end of sequence), block-mask row qi (as a shared-memory bitmap;
+// nullptr: no block mask).
 struct KTileIter {
-  const uint8_t* row;  // block-mask row or nullptr
+  const uint32_t* bits;
   int jend;
-  __device__ int next(int j) const {
-    if (row)
-      while (j < jend && row[j] == 0) ++j;
-    return j;
-  }
+  __device__ int next(int j) const { return bits ? next_tile_bit(bits, j, jend) : j; }
 };
 
 template <int D>
@@ -97,6 +94,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   __shared__ uint64_t v_full[C::kVStages], dp_full[C::kVStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask row qi
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lin = blockIdx.x;
@@ -107,10 +105,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const int jkv = (kv_limit + 127) / 128;
-  const KTileIter ktiles{p.block_mask ? p.block_mask + (size_t)qi * p.T : nullptr,
-                         p.causal ? min(jkv, qi + 1) : jkv};
-  const int jfirst = ktiles.next(0);
-  const bool any = jfirst < ktiles.jend;
+  if (p.block_mask) build_tile_bitmap(mask_bits, p.block_mask + (size_t)qi * p.T, 1, p.T);
+  const KTileIter ktiles{p.block_mask ? mask_bits : nullptr, p.causal ? min(jkv, qi + 1) : jkv};
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
@@ -136,6 +132,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  const int jfirst = ktiles.next(0);  // after the barrier: the bitmap is complete
+  const bool any = jfirst < ktiles.jend;
 
   if (warp == C::kMathWarps) {
     // ------------------------------------------------------------ producer

@@ -71,16 +71,13 @@ struct BwdParams {
   int* status;
 };
 
-// Query tiles i that see key tile kt: i in [ibegin, T), block-mask column kt.
+// Query tiles i that see key tile kt: i in [ibegin, T), block-mask column kt
+// (as a shared-memory bitmap; nullptr: no block mask).
 struct QTileIter {
-  const uint8_t* mask;  // block mask base or nullptr
-  int T, kt, ibegin;
+  const uint32_t* bits;
+  int T, ibegin;
   __device__ int first() const { return next(ibegin); }
-  __device__ int next(int i) const {
-    if (mask)
-      while (i < T && mask[(size_t)i * T + kt] == 0) ++i;
-    return i;
-  }
+  __device__ int next(int i) const { return bits ? next_tile_bit(bits, i, T) : i; }
 };
 
 __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, int n) {
@@ -116,6 +113,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __shared__ __align__(16) float s_nD[128];   // -D
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask column kt
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lin = blockIdx.x;
@@ -126,7 +124,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const bool keys_live = kt * 128 < kv_limit;  // else every key of the tile is padding
-  const QTileIter qtiles{p.block_mask, p.T, kt, p.causal ? kt : 0};
+  if (p.block_mask) build_tile_bitmap(mask_bits, p.block_mask + kt, (size_t)p.T, p.T);
+  const QTileIter qtiles{p.block_mask ? mask_bits : nullptr, p.T, p.causal ? kt : 0};
   const int iend = keys_live ? p.T : 0;
 
   if (tid == 0) {

@@ -130,6 +130,40 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, i
                : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Block-sparse tile masks.  A CTA copies the row (or column) of the caller's
+// uint8 [T, T] tile mask it walks into a shared-memory bitmap once, so that
+// finding the next visible tile is a few bit scans instead of a chain of
+// dependent global loads (one per skipped tile).
+// ---------------------------------------------------------------------------
+constexpr int kMaskBitmapWords = 128;  // tiles per bitmap: 4096 (N <= 524288)
+
+// bits[t / 32] bit t % 32 = (first[t * stride] != 0), t < T.  Every thread of
+// the CTA takes part (whole warps); a __syncthreads must follow before use.
+__device__ __forceinline__ void build_tile_bitmap(uint32_t* bits, const uint8_t* first,
+                                                  size_t stride, int T) {
+  const int warps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int w = warp; w < (T + 31) / 32; w += warps) {
+    const int t = 32 * w + lane;
+    const uint32_t on = __ballot_sync(0xffffffffu, t < T && first[(size_t)t * stride] != 0);
+    if (lane == 0) bits[w] = on;
+  }
+}
+
+__device__ __forceinline__ bool tile_bit(const uint32_t* bits, int t) {
+  return (bits[t >> 5] >> (t & 31)) & 1u;
+}
+
+// The first t' >= t with bit t' set, or `end` if there is none below end.
+__device__ __forceinline__ int next_tile_bit(const uint32_t* bits, int t, int end) {
+  while (t < end) {
+    const uint32_t w = bits[t >> 5] >> (t & 31);
+    if (w) return min(t + __ffs(w) - 1, end);
+    t = (t | 31) + 1;
+  }
+  return end;
+}
+
 // One arrival for the whole warp, made by lane 0 once every lane has got
 // here: the lanes' earlier writes (completed TMEM stores, shared-memory
 // stores fenced for the async proxy) are ordered before it by the warp sync.

@@ -63,15 +63,17 @@ struct FwdParams {
 
 // Visibility of key tile j for the CTA's two query tiles.
 struct PairTiles {
-  const uint8_t* row_a;  // block-mask rows (nullptr: no block mask)
-  const uint8_t* row_b;
-  int jend_a, jend_b;    // tiles j >= jend are invisible (causal / key padding / past N)
-  __device__ bool vis_a(int j) const { return j < jend_a && (!row_a || row_a[j]); }
-  __device__ bool vis_b(int j) const { return j < jend_b && (!row_b || row_b[j]); }
-  __device__ int next(int j) const {  // next key tile visible to either tile
-    const int jend = max(jend_a, jend_b);
-    while (j < jend && !vis_a(j) && !vis_b(j)) ++j;
-    return j;
+  const uint32_t* bits_a;  // block-mask rows as shared-memory bitmaps (nullptr: no block mask)
+  const uint32_t* bits_b;
+  int jend_a, jend_b;      // tiles j >= jend are invisible (causal / key padding / past N)
+  __device__ bool vis_a(int j) const { return j < jend_a && (!bits_a || tile_bit(bits_a, j)); }
+  __device__ bool vis_b(int j) const { return j < jend_b && (!bits_b || tile_bit(bits_b, j)); }
+  __device__ int next(int j) const {  // next key tile visible to either tile, or end()
+    if (!bits_a) return j;            // no block mask: every j < end() is visible to one
+    const int na = next_tile_bit(bits_a, j, jend_a);
+    const int nb = bits_b ? next_tile_bit(bits_b, j, jend_b) : jend_b;
+    const int ea = na < jend_a ? na : end(), eb = nb < jend_b ? nb : end();
+    return min(ea, eb);
   }
   __device__ int end() const { return max(jend_a, jend_b); }
 };
@@ -193,6 +195,7 @@ __global__ void __launch_bounds__(352, 1)
       v_empty[C::kStages];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ uint32_t mask_bits[2][kMaskBitmapWords];  // block-mask rows qa, qb
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest pairs first (causal rows near the end see the most keys)
@@ -208,8 +211,12 @@ __global__ void __launch_bounds__(352, 1)
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const int jkv = (kv_limit + 127) / 128;
   PairTiles tiles;
-  tiles.row_a = p.block_mask ? p.block_mask + (size_t)qa * p.T : nullptr;
-  tiles.row_b = (p.block_mask && has_b) ? p.block_mask + (size_t)qb * p.T : nullptr;
+  tiles.bits_a = p.block_mask ? mask_bits[0] : nullptr;
+  tiles.bits_b = (p.block_mask && has_b) ? mask_bits[1] : nullptr;
+  if (p.block_mask) {
+    build_tile_bitmap(mask_bits[0], p.block_mask + (size_t)qa * p.T, 1, p.T);
+    if (has_b) build_tile_bitmap(mask_bits[1], p.block_mask + (size_t)qb * p.T, 1, p.T);
+  }
   tiles.jend_a = p.causal ? min(jkv, qa + 1) : jkv;
   tiles.jend_b = !has_b ? 0 : (p.causal ? min(jkv, qb + 1) : jkv);
 

@@ -73,6 +73,7 @@ typedef struct {
   const int32_t* kv_len;     /* KEY_PADDING: device int32 [B]; values are clamped   */
                              /* to 0..N (0 = every key of the batch is padding)     */
   const uint8_t* block_mask; /* BLOCK_SPARSE: device uint8 [T*T], T = ceil(N/128)   */
+                             /* <= 4096 (N <= 524288; FA_ERR_UNSUPPORTED beyond)    */
   int block_size;            /* BLOCK_SPARSE: tile edge of block_mask, must be 128  */
 } fa_mask;
 

@@ -64,8 +64,9 @@ __all__ = [
 # masks
 # --------------------------------------------------------------------------
 
-def visible(rows, n_keys, causal=False, kv_len_b=None, block_mask=None, block=128):
-    """Boolean visibility of keys 0..n_keys-1 from the given query rows.
+def visible(rows, n_keys, causal=False, kv_len_b=None, block_mask=None, block=128, keys=None):
+    """Boolean visibility of keys 0..n_keys-1 (or of the key indices `keys`)
+    from the given query rows.
 
     rows      : 1-D integer array of query indices (or an int N for 0..N-1)
     causal    : keep j <= i (lower-triangular mask, GitHub issue #941)
@@ -75,8 +76,9 @@ def visible(rows, n_keys, causal=False, kv_len_b=None, block_mask=None, block=12
     if np.isscalar(rows):
         rows = np.arange(int(rows))
     rows = np.asarray(rows, dtype=np.int64)
-    cols = np.arange(n_keys, dtype=np.int64)
-    vis = np.ones((rows.size, n_keys), dtype=bool)
+    cols = (np.arange(n_keys, dtype=np.int64) if keys is None
+            else np.asarray(keys, dtype=np.int64))
+    vis = np.ones((rows.size, cols.size), dtype=bool)
     if causal:
         vis &= cols[None, :] <= rows[:, None]
     if kv_len_b is not None:
@@ -247,8 +249,7 @@ def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=No
             c = cols[b, h]
             qf = np.asarray(q[b, h], np.float64)
             dof = np.asarray(do[b, h], np.float64)
-            vis_all = visible(rows, N, causal, _kv_len_of(kv_len, b), block_mask, block)
-            vis = vis_all[:, c]
+            vis = visible(rows, N, causal, _kv_len_of(kv_len, b), block_mask, block, keys=c)
             s = scores(qf, k[b, h][c], scale, vis)                  # [N, C]
             l = lse[b, h][:, None]
             with np.errstate(invalid="ignore"):

@@ -101,6 +101,9 @@ def test_fwd_rejects_bad_masks(fa):
     assert fwd(fa, mask=m) == 1   # NULL block mask
     m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 64))
     assert fwd(fa, mask=m) == 2   # only 128-wide tiles
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 128))
+    assert fwd(fa, mask=m, N=4096 * 128) == 5       # T = 4096: valid (no CUDA here)
+    assert fwd(fa, mask=m, N=4096 * 128 + 1) == 2   # T = 4097: beyond the tile bitmap
 
 
 def bwd(fa, **kw):

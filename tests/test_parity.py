@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import WORKLOADS, generate, random_case
+from workloads import WORKLOADS, block_mask_pattern, generate, random_case
 from _gpu_helpers import TOL, f64, max_abs, rel_fro, run, to_device
 
 pytestmark = pytest.mark.gpu
@@ -135,7 +135,8 @@ KEY_HEADS = 2
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["long_causal_d128", "block_sparse"])
+@pytest.mark.parametrize("name", ["long_causal_d128", "block_sparse", "sparse_local_global",
+                                  "sparse_butterfly"])
 def test_workload_sampled(fa, name):
     w = WORKLOADS[name]
     case = generate(w)
@@ -165,6 +166,63 @@ def test_workload_sampled(fa, name):
     assert max_abs(lse.cpu().numpy().astype(np.float64)[sl], lse_all) <= tl
     # any size: shifting every key by one vector leaves O unchanged, so the
     # key gradients of each head sum to zero (bf16 rounding allows a little)
+    dk64 = f64(dk)
+    tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
+    per = np.linalg.norm(dk64, axis=(2, 3))
+    assert np.all(tot <= 2e-2 * per)
+
+
+@pytest.mark.parametrize("pattern", ["local", "local_global", "strided", "butterfly"])
+@pytest.mark.parametrize("d,causal", [(64, False), (128, True)])
+def test_sparse_patterns(fa, pattern, d, causal):
+    """Every structured tile pattern, all rows against the oracle (T = 16)."""
+    B, H, N = 1, 2, 2048 - 37   # ragged last tile
+    T = (N + 127) // 128
+    case = random_case(B, H, N, d, seed=sum(map(ord, pattern)) + d,
+                       block_mask=block_mask_pattern(pattern, T))
+    check_full(fa, case, B, H, N, d, causal, "bf16")
+
+
+@pytest.mark.slow
+def test_path256_butterfly(fa):
+    """Path-256 length (65536 tokens) under the butterfly tile mask: sampled
+    query rows, and every row of one key tile exactly (the oracle needs the
+    statistics of just the query tiles that see it)."""
+    B, H, N, d = 1, 2, 65536, 64
+    T = N // 128
+    bm = block_mask_pattern("butterfly", T)
+    case = random_case(B, H, N, d, seed=256, block_mask=bm)
+    scale = d ** -0.5
+    t = to_device(case, "bf16")
+    o, lse, (dq, dk, dv) = run(fa, t, scale, False)
+    to, tl, tg = TOL["bf16"]
+    kw = dict(block_mask=bm)
+    rng = np.random.default_rng(256)
+    rows = np.stack([np.stack([np.sort(rng.choice(N, 256, replace=False)) for _ in range(H)])
+                     for _ in range(B)])
+    take = lambda a, r: np.take_along_axis(a, r[..., None], axis=2)
+    ro, rl = oracle.forward_rows(case["q"], case["k"], case["v"], scale, rows, **kw)
+    assert max_abs(take(f64(o), rows), ro) <= to
+    assert max_abs(np.take_along_axis(lse.cpu().numpy().astype(np.float64), rows, axis=2),
+                   rl) <= tl
+    rdq = oracle.backward_query_rows(case["q"], case["k"], case["v"], case["do"], scale, rows,
+                                     **kw)
+    assert rel_fro(take(f64(dq), rows), rdq) <= tg
+    kt = 300
+    seen_by = np.flatnonzero(bm[:, kt])
+    qrows = np.concatenate([np.arange(i * 128, i * 128 + 128) for i in seen_by])
+    qrows = np.broadcast_to(qrows, (B, H, qrows.size)).copy()
+    so, sl = oracle.forward_rows(case["q"], case["k"], case["v"], scale, qrows, **kw)
+    lse_all = np.zeros((B, H, N))
+    d_all = np.zeros((B, H, N))
+    np.put_along_axis(lse_all, qrows, sl, axis=2)
+    do_rows = np.take_along_axis(np.asarray(case["do"], np.float64), qrows[..., None], axis=2)
+    np.put_along_axis(d_all, qrows, np.sum(do_rows * so, -1), axis=2)
+    keys = np.broadcast_to(np.arange(kt * 128, kt * 128 + 128), (B, H, 128)).copy()
+    rdk, rdv = oracle.backward_key_rows(case["q"], case["k"], case["v"], case["do"], scale, keys,
+                                        lse_all, d_all, **kw)
+    assert rel_fro(f64(dk)[..., kt * 128:kt * 128 + 128, :], rdk) <= tg
+    assert rel_fro(f64(dv)[..., kt * 128:kt * 128 + 128, :], rdv) <= tg
     dk64 = f64(dk)
     tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
     per = np.linalg.norm(dk64, axis=(2, 3))

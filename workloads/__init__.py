@@ -8,7 +8,7 @@ The workloads stand in for the workloads of the FlashAttention paper (summary
 page "FlashAttention: Fast and Memory-Efficient Exact Attention with
 IO-Awareness", section "Results": GPT-2 at sequence length 1K, BERT-large at
 512, long-context causal models up to 64K tokens, block-sparse attention on
-long sequences),
+long sequences up to the 64K tokens of Path-256),
 whose datasets and weights are not available: only the shapes, masks and value
 distributions are reproduced.
 
@@ -19,7 +19,9 @@ Recipe (every workload, seed 0 unless stated):
   then rounded to bf16 with round-to-nearest-even (fp32 workloads keep fp32);
   then kv_len = rng.integers(128, 513, B)           (key-padding workload)
   then tile mask = rng.random((T, T)) < 0.125, diagonal forced to 1
-                                                    (block-sparse workload)
+                                    (block-sparse workloads, pattern "random";
+                                     the other patterns draw nothing, see
+                                     block_mask_pattern)
   then sampled rows: per (b, h), rng.choice(N, 256, replace=False) for query
   rows, then the same for key rows (long workloads only).
 """
@@ -44,6 +46,7 @@ class Workload:
     sampled: bool = False  # check on sampled rows instead of every row
     block: int = 128
     sparse_p: float = 0.125
+    pattern: str = "random"  # tile-mask pattern of block-sparse workloads
 
     @property
     def scale(self):
@@ -68,6 +71,15 @@ WORKLOADS = {
     # block-sparse attention on long sequences
     "block_sparse": Workload("block_sparse", 2, 16, 16384, 64, "bf16", False, "block_sparse",
                              sampled=True),
+    # the same sequences under structured tile masks (the pages fix no pattern;
+    # these are common fixed patterns, see block_mask_pattern)
+    "sparse_local_global": Workload("sparse_local_global", 2, 16, 16384, 64, "bf16", False,
+                                    "block_sparse", sampled=True, pattern="local_global"),
+    "sparse_butterfly": Workload("sparse_butterfly", 2, 16, 16384, 64, "bf16", False,
+                                 "block_sparse", sampled=True, pattern="butterfly"),
+    # Path-256 length (a 256 x 256 image as 65536 tokens) under a butterfly mask
+    "path256_butterfly": Workload("path256_butterfly", 1, 8, 65536, 64, "bf16", False,
+                                  "block_sparse", sampled=True, pattern="butterfly"),
     # 64K-token causal context (the pages' longest dense sequences), head dim 128
     "causal_64k_d128": Workload("causal_64k_d128", 1, 4, 65536, 128, "bf16", True, "none",
                                 value_scale=0.5, sampled=True),
@@ -110,10 +122,7 @@ def generate(w, seed=0, samples=256):
     if w.mask == "key_padding":
         out["kv_len"] = rng.integers(128, 513, w.B).astype(np.int32)
     if w.mask == "block_sparse":
-        T = w.tiles
-        bm = rng.random((T, T)) < w.sparse_p
-        bm[np.arange(T), np.arange(T)] = True
-        out["block_mask"] = bm.astype(np.uint8)
+        out["block_mask"] = block_mask_pattern(w.pattern, w.tiles, rng, w.sparse_p)
     if w.sampled:
         rows = np.zeros((w.B, w.H, samples), np.int64)
         cols = np.zeros((w.B, w.H, samples), np.int64)
@@ -125,6 +134,42 @@ def generate(w, seed=0, samples=256):
                 cols[b, h] = rng.choice(w.N, samples, replace=False)
         out["rows"], out["cols"] = rows, cols
     return out
+
+
+PATTERNS = ("random", "local", "local_global", "strided", "butterfly")
+
+
+def block_mask_pattern(pattern, T, rng=None, p=0.125):
+    """uint8 [T, T] tile mask (1 = tile computed) of a fixed sparsity pattern.
+
+    The pages define block-sparse attention for any predefined tile mask
+    (summary page, "Extension: Block-Sparse FlashAttention") and name none;
+    these are common choices:
+      random       each tile kept with probability p (draws rng.random((T, T)))
+      local        a band: |i - j| <= 2 tiles
+      local_global the band |i - j| <= 1 plus tile row 0 and tile column 0
+      strided      the band |i - j| <= 1 plus every 8th tile column (j % 8 == 7)
+      butterfly    j == i or i XOR j a power of two (the union of the supports
+                   of the butterfly factors of a T x T butterfly matrix)
+    The diagonal is always kept, so every query row sees at least its own tile."""
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    if pattern == "random":
+        m = rng.random((T, T)) < p
+    elif pattern == "local":
+        m = np.abs(i - j) <= 2
+    elif pattern == "local_global":
+        m = (np.abs(i - j) <= 1) | (i == 0) | (j == 0)
+    elif pattern == "strided":
+        m = (np.abs(i - j) <= 1) | (j % 8 == 7)
+    elif pattern == "butterfly":
+        x = i ^ j
+        m = (x & (x - 1)) == 0   # 0 or a single bit
+    else:
+        raise ValueError("unknown pattern %r" % pattern)
+    m = np.array(m, dtype=bool)
+    m[np.arange(T), np.arange(T)] = True
+    return m.astype(np.uint8)
 
 
 def random_case(B, H, N, d, seed, dtype="bf16", value_scale=1.0, kv_len=None,
