@@ -5,6 +5,7 @@ may import this package.  The product path (the CUDA library and its Python
 binding) never imports, links or calls anything here, and this package imports
 nothing from the product path.
 """
+from . import dropout  # noqa: F401
 from .attention import (  # noqa: F401
     visible,
     scores,

@@ -45,12 +45,18 @@ Readings taken where the pages are silent:
   * the block-sparse tile mask is one T x T 0/1 array shared by every (b, h),
     T = ceil(N / block).
 
+Dropout (optional argument `dropout=(p, seed, offset)` of the whole-tensor and
+sampled-row functions) follows `oracle/dropout.py`: O = (P o Z) V / (1 - p)
+with the mask Z of that module, and the chain rule through it.
+
 Rows of the score matrix are independent by definition, so functions that
 handle long sequences evaluate whole rows a group of rows at a time; nothing
 else is blocked, fused or reordered.  All arithmetic is float64 on inputs that
 the caller has already rounded to the precision the GPU sees.
 """
 import numpy as np
+
+from . import dropout as _dropout
 
 __all__ = [
     "visible", "scores", "probabilities", "forward", "backward",
@@ -121,19 +127,32 @@ def probabilities(s):
     return p, lse
 
 
-def _slice_forward(q, k, v, scale, vis):
+def _drop(dropout, rows, cols, bh):
+    """(Z, scale) of the dropout mask for query `rows` x key `cols` of head
+    bh, or (None, 1) without dropout."""
+    if dropout is None or _dropout.threshold(dropout[0]) == 0:
+        return None, 1.0
+    p, seed, offset = dropout
+    return _dropout.keep_mask(rows, cols, bh, p, seed, offset), _dropout.keep_scale(p)
+
+
+def _slice_forward(q, k, v, scale, vis, z=None, rp=1.0):
     p, lse = probabilities(scores(q, k, scale, vis))
-    return p @ np.asarray(v, np.float64), lse, p
+    pd = p if z is None else p * z * rp
+    return pd @ np.asarray(v, np.float64), lse, p
 
 
-def _slice_backward(q, k, v, do, scale, vis):
+def _slice_backward(q, k, v, do, scale, vis, z=None, rp=1.0):
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     do = np.asarray(do, np.float64)
     p, _ = probabilities(scores(q, k, scale, vis))
-    dv = p.T @ do
+    pd = p if z is None else p * z * rp
+    dv = pd.T @ do
     dp = do @ v.T
+    if z is not None:
+        dp = dp * z * rp
     d_row = np.sum(p * dp, axis=1)
     ds = p * (dp - d_row[:, None])
     dq = scale * (ds @ k)
@@ -145,7 +164,8 @@ def _slice_backward(q, k, v, do, scale, vis):
 # whole tensors [B, H, N, d]
 # --------------------------------------------------------------------------
 
-def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, block=128):
+def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, block=128,
+            dropout=None):
     """O [B,H,N,d] and lse [B,H,N] (natural log) for q, k, v of shape [B,H,N,d]."""
     B, H, N, d = q.shape
     o = np.zeros((B, H, N, d), np.float64)
@@ -153,11 +173,13 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, block=12
     for b in range(B):
         vis = visible(N, k.shape[2], causal, _kv_len_of(kv_len, b), block_mask, block)
         for h in range(H):
-            o[b, h], lse[b, h], _ = _slice_forward(q[b, h], k[b, h], v[b, h], scale, vis)
+            z, rp = _drop(dropout, np.arange(N), np.arange(k.shape[2]), b * H + h)
+            o[b, h], lse[b, h], _ = _slice_forward(q[b, h], k[b, h], v[b, h], scale, vis, z, rp)
     return o, lse
 
 
-def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, block=128):
+def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, block=128,
+             dropout=None):
     """(dQ, dK, dV, D) for the loss sum(O * dO); D [B,H,N] = rowsum(P o dP)."""
     B, H, N, d = q.shape
     dq = np.zeros((B, H, N, d), np.float64)
@@ -167,8 +189,9 @@ def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, blo
     for b in range(B):
         vis = visible(N, k.shape[2], causal, _kv_len_of(kv_len, b), block_mask, block)
         for h in range(H):
+            z, rp = _drop(dropout, np.arange(N), np.arange(k.shape[2]), b * H + h)
             dq[b, h], dk[b, h], dv[b, h], dd[b, h] = _slice_backward(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, vis)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, vis, z, rp)
     return dq, dk, dv, dd
 
 
@@ -177,7 +200,7 @@ def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, blo
 # --------------------------------------------------------------------------
 
 def forward_rows(q, k, v, scale, rows, causal=False, kv_len=None, block_mask=None,
-                 block=128):
+                 block=128, dropout=None):
     """O and lse of the selected query rows; rows: int array [B,H,R]."""
     B, H, N, d = q.shape
     R = rows.shape[2]
@@ -186,13 +209,14 @@ def forward_rows(q, k, v, scale, rows, causal=False, kv_len=None, block_mask=Non
     for b in range(B):
         for h in range(H):
             vis = visible(rows[b, h], N, causal, _kv_len_of(kv_len, b), block_mask, block)
+            z, rp = _drop(dropout, rows[b, h], np.arange(N), b * H + h)
             o[b, h], lse[b, h], _ = _slice_forward(q[b, h][rows[b, h]], k[b, h],
-                                                   v[b, h], scale, vis)
+                                                   v[b, h], scale, vis, z, rp)
     return o, lse
 
 
 def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
-                        block_mask=None, block=128):
+                        block_mask=None, block=128, dropout=None):
     """dQ of the selected query rows.  Everything dQ_i needs is in row i:
     P_i., dP_i. = dO_i V^T, D_i = sum_j P_ij dP_ij."""
     B, H, N, d = q.shape
@@ -204,6 +228,9 @@ def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
             vis = visible(r, N, causal, _kv_len_of(kv_len, b), block_mask, block)
             p, _ = probabilities(scores(q[b, h][r], k[b, h], scale, vis))
             dp = np.asarray(do[b, h][r], np.float64) @ np.asarray(v[b, h], np.float64).T
+            z, rp = _drop(dropout, r, np.arange(N), b * H + h)
+            if z is not None:
+                dp = dp * z * rp
             d_row = np.sum(p * dp, axis=1)
             ds = p * (dp - d_row[:, None])
             dq[b, h] = scale * (ds @ np.asarray(k[b, h], np.float64))
@@ -211,7 +238,7 @@ def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
 
 
 def row_stats(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None,
-              block=128, rows_per_group=1024):
+              block=128, rows_per_group=1024, dropout=None):
     """lse_i and D_i = sum_j P_ij dP_ij for EVERY query row, [B,H,N] each.
 
     Rows are taken a group at a time so that the score rows of a long
@@ -228,12 +255,15 @@ def row_stats(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None,
                 vis = visible(r, N, causal, _kv_len_of(kv_len, b), block_mask, block)
                 p, lse[b, h, r] = probabilities(scores(q[b, h][r], kf, scale, vis))
                 dp = np.asarray(do[b, h][r], np.float64) @ vf.T
+                z, rp = _drop(dropout, r, np.arange(N), b * H + h)
+                if z is not None:
+                    dp = dp * z * rp
                 dd[b, h, r] = np.sum(p * dp, axis=1)
     return lse, dd
 
 
 def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=None,
-                      block_mask=None, block=128):
+                      block_mask=None, block=128, dropout=None):
     """dK and dV of the selected key rows (cols: int array [B,H,C]).
 
     dK_j and dV_j sum over every query row, so they need every row's lse and
@@ -255,8 +285,13 @@ def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=No
             with np.errstate(invalid="ignore"):
                 p = np.where(vis & np.isfinite(l), np.exp(s - np.where(np.isfinite(l), l, 0.0)), 0.0)
             dp = dof @ np.asarray(v[b, h][c], np.float64).T         # [N, C]
+            z, rp = _drop(dropout, rows, c, b * H + h)
+            pd = p
+            if z is not None:
+                dp = dp * z * rp
+                pd = p * z * rp
             ds = p * (dp - dd[b, h][:, None])
-            dv[b, h] = p.T @ dof
+            dv[b, h] = pd.T @ dof
             dk[b, h] = scale * (ds.T @ qf)
     return dk, dv
 
