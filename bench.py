@@ -153,6 +153,8 @@ def run_gpu(args, rank, world, local_rank):
     kv_len = None if case["kv_len"] is None else torch.from_numpy(case["kv_len"]).to(dev)
     bmask = None if case["block_mask"] is None else torch.from_numpy(case["block_mask"]).to(dev)
     mask = fa.make_mask(kv_len, bmask)
+    # fused dropout (--dropout p): the same kernels with the mask drawn in them
+    opt = fa.make_options(None, args.dropout, 0x5EED, 1) if args.dropout else None
     kept = kept_fraction(case["block_mask"])
     fwd_flops, step_flops = flops(w, kept)
     # secondary FLOP figures, labelled: dense-equivalent for block-sparse (every
@@ -195,16 +197,17 @@ def run_gpu(args, rank, world, local_rank):
                 ev[name].append((a, b))
             else:
                 fn()
-        mark("fwd", lambda: fa.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, stream))
+        mark("fwd", lambda: fa.fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, opt,
+                                         stream))
         mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
         dq_stream = stream if record else stream2
         if not record:
             ev_pre.record(stream)
             stream2.wait_event(ev_pre)
-        mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv(q, k, v, do, lse, D, dk, dv, B, H, N, d, scale,
-                                                w.causal, mask, stream))
-        mark("bwd_dq", lambda: fa.fa_bwd_dq(q, k, v, do, lse, D, dq, B, H, N, d, scale, w.causal,
-                                            mask, dq_stream))
+        mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv_ex(q, k, v, do, lse, D, dk, dv, B, H, N, d, scale,
+                                                   w.causal, mask, opt, stream))
+        mark("bwd_dq", lambda: fa.fa_bwd_dq_ex(q, k, v, do, lse, D, dq, B, H, N, d, scale,
+                                               w.causal, mask, opt, dq_stream))
         if not record:
             ev_dq.record(stream2)
             stream.wait_event(ev_dq)  # the next step's forward rewrites o and lse
@@ -277,7 +280,8 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) x %g, bf16)" % w.value_scale,
         "config": {
             "workload": w.name, "B": B, "H": H, "N": N, "d": d, "causal": w.causal,
-            "mask": w.mask, "kept_tile_fraction": kept, "global_batch": B * world,
+            "mask": w.mask, "kept_tile_fraction": kept, "dropout": args.dropout,
+            "global_batch": B * world,
             "seq_len": N, "parallelism": "replicas" if world > 1 else "single GPU",
             "l2": "inputs (Q,K,V,dO = %d MiB) larger than the 129 MB L2; no flush" %
                   (4 * q.numel() * 2 >> 20),
@@ -314,11 +318,11 @@ def run_gpu(args, rank, world, local_rank):
             "value": round(world * eff_step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "note": "sum_b N * kv_len[b] in place of B * N^2"}
     if not args.no_extras:
-        result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args)
+        result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt)
     return result
 
 
-def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
+def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None):
     """Same metric through the public API with host buffers: every step copies
     its inputs in from pinned host memory, runs fa_fwd and the three backward
     steps (dQ on a second stream, as in the device-resident steps) and copies
@@ -364,15 +368,15 @@ def run_e2e(fa, torch, dev, case, w, mask, step_flops, args):
         s_comp.wait_event(in_ready[k % 2])
         if k >= 2:
             s_comp.wait_event(out_done[k % 2])  # step k-2's results have left this set
-        fa.fa_fwd(x["q"], x["k"], x["v"], y["o"], y["lse"], B, H, N, d, w.scale, w.causal, mask,
-                  s_comp)
+        fa.fa_fwd_ex(x["q"], x["k"], x["v"], y["o"], y["lse"], B, H, N, d, w.scale, w.causal, mask,
+                     opt, s_comp)
         fa.fa_bwd_preprocess(y["o"], x["do"], D, B, H, N, d, s_comp)
         ev_pre.record(s_comp)
         s_dq.wait_event(ev_pre)
-        fa.fa_bwd_dkdv(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dk"], y["dv"], B, H, N, d,
-                       w.scale, w.causal, mask, s_comp)
-        fa.fa_bwd_dq(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dq"], B, H, N, d, w.scale,
-                     w.causal, mask, s_dq)
+        fa.fa_bwd_dkdv_ex(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dk"], y["dv"], B, H, N,
+                          d, w.scale, w.causal, mask, opt, s_comp)
+        fa.fa_bwd_dq_ex(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dq"], B, H, N, d,
+                        w.scale, w.causal, mask, opt, s_dq)
         ev_dq.record(s_dq)
         s_comp.wait_event(ev_dq)
         comp_done[k % 2].record(s_comp)
@@ -486,6 +490,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-extras", action="store_true",
                     help="skip e2e and the CPU baseline (for profiler runs)")
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="fused dropout probability on the attention probabilities (0: none)")
     ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--reference-rows", type=int, default=2048)
     args = ap.parse_args()

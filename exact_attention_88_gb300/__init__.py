@@ -7,7 +7,8 @@ kernels of libfa.so.  The C functions keep their names (`fa_fwd`, `fa_bwd`,
 allocate the outputs with torch and call the same C functions; they accept
 [B, H, N, d] views of any layout whose last dimension is contiguous (for
 example a [B, N, H, d] buffer transposed to [B, H, N, d]) and pass each
-tensor's strides to the *_strided calls, so nothing is copied.
+tensor's strides to the *_ex calls, so nothing is copied; they also take
+dropout (probability, seed, offset).
 
 Importing this package fails loudly if libfa.so has not been built
 (`python -c "import __graft_entry__ as g; g.build()"`): there is no fallback.
@@ -16,8 +17,9 @@ import ctypes
 import os
 
 __all__ = [
-    "FaError", "FaMask", "FaLayout", "FaLayouts", "layout_of", "make_layouts",
-    "fa_fwd_strided", "fa_bwd_strided", "fa_fwd_fp32_strided", "fa_bwd_fp32_strided",
+    "FaError", "FaMask", "FaLayout", "FaLayouts", "FaDropout", "FaOptions", "layout_of",
+    "make_layouts", "make_options", "fa_fwd_ex", "fa_bwd_ex", "fa_fwd_fp32_ex", "fa_bwd_fp32_ex",
+    "fa_bwd_preprocess_ex", "fa_bwd_dkdv_ex", "fa_bwd_dq_ex", "fa_debug_dropout_mask",
     "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_fwd_fp32", "fa_bwd_fp32",
     "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
@@ -59,6 +61,16 @@ class FaLayouts(ctypes.Structure):
     _fields_ = [(n, FaLayout) for n in _LAYOUT_NAMES]
 
 
+class FaDropout(ctypes.Structure):
+    """Dropout of a call (fa_dropout): probability, generator seed, offset."""
+    _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint32)]
+
+
+class FaOptions(ctypes.Structure):
+    """Options of the *_ex calls (fa_options)."""
+    _fields_ = [("layouts", ctypes.POINTER(FaLayouts)), ("dropout", ctypes.POINTER(FaDropout))]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError("libfa.so is not built (expected at %s); run "
                       "__graft_entry__.build() first" % LIB_PATH)
@@ -69,7 +81,7 @@ _i = ctypes.c_int
 _f = ctypes.c_float
 _sz = ctypes.c_size_t
 _mp = ctypes.POINTER(FaMask)
-_lp = ctypes.POINTER(FaLayouts)
+_op = ctypes.POINTER(FaOptions)
 
 _SIGS = {
     "fa_fwd": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _p],
@@ -86,10 +98,14 @@ _SIGS = {
     "fa_debug_wait_timeout": [ctypes.c_uint, _p],
     "fa_bwd_noalloc": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_last_cuda_error": [],
-    "fa_fwd_strided": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
-    "fa_fwd_fp32_strided": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
-    "fa_bwd_strided": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
-    "fa_bwd_fp32_strided": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _lp, _p],
+    "fa_fwd_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_fwd_fp32_ex": [_p, _p, _p, _p, _p, _i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_bwd_ex": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_bwd_fp32_ex": [_p] * 10 + [_sz, _i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_bwd_preprocess_ex": [_p, _p, _p, _i, _i, _i, _i, _op, _p],
+    "fa_bwd_dkdv_ex": [_p] * 8 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_bwd_dq_ex": [_p] * 7 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_debug_dropout_mask": [_p, _i, _i, _i, ctypes.POINTER(FaDropout), _i, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -144,45 +160,87 @@ def layout_of(t):
 
 
 def make_layouts(**tensors):
-    """A pointer to an FaLayouts holding layout_of(t) for each named tensor
-    (names: q, k, v, o, dO, dq, dk, dv); entries not given stay zero, which
-    the calls that read them reject."""
+    """An FaLayouts holding layout_of(t) for each named tensor (names: q, k,
+    v, o, dO, dq, dk, dv); entries not given stay zero, which the calls that
+    read them reject."""
     unknown = set(tensors) - set(_LAYOUT_NAMES)
     if unknown:
         raise ValueError("unknown tensor names: %s" % sorted(unknown))
     ls = FaLayouts()
     for name, t in tensors.items():
         setattr(ls, name, layout_of(t))
-    return ctypes.pointer(ls)
+    return ls
 
 
-def fa_fwd_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, layouts=None,
+def make_options(layouts=None, dropout_p=0.0, seed=0, offset=0):
+    """A pointer to an FaOptions: `layouts` an FaLayouts (or None: dense),
+    dropout with probability dropout_p (0: none), generator seed and offset.
+    The pointer keeps its members alive."""
+    opt = FaOptions()
+    keep = []
+    if layouts is not None:
+        keep.append(layouts)
+        opt.layouts = ctypes.pointer(layouts)
+    if dropout_p:
+        dr = FaDropout(dropout_p, seed, offset)
+        keep.append(dr)
+        opt.dropout = ctypes.pointer(dr)
+    ptr = ctypes.pointer(opt)
+    ptr._keep = keep
+    return ptr
+
+
+def fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, options=None,
+              stream=None):
+    _check(lib.fa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                         int(causal), mask, options, _stream(stream)), "fa_fwd_ex")
+
+
+def fa_fwd_fp32_ex(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, options=None,
                    stream=None):
-    _check(lib.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
-                              int(causal), mask, layouts, _stream(stream)), "fa_fwd_strided")
+    _check(lib.fa_fwd_fp32_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
+                              int(causal), mask, options, _stream(stream)), "fa_fwd_fp32_ex")
 
 
-def fa_fwd_fp32_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, layouts=None,
-                        stream=None):
-    _check(lib.fa_fwd_fp32_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                   scale, int(causal), mask, layouts, _stream(stream)),
-           "fa_fwd_fp32_strided")
+def fa_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
+              causal, mask=None, options=None, stream=None):
+    _check(lib.fa_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+                         _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, B, H, N, d, scale,
+                         int(causal), mask, options, _stream(stream)), "fa_bwd_ex")
 
 
-def fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
-                   scale, causal, mask=None, layouts=None, stream=None):
-    _check(lib.fa_bwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
+def fa_bwd_fp32_ex(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                   scale, causal, mask=None, options=None, stream=None):
+    _check(lib.fa_bwd_fp32_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse), _ptr(dq),
                               _ptr(dk), _ptr(dv), _ptr(workspace), workspace_bytes, B, H, N, d,
-                              scale, int(causal), mask, layouts, _stream(stream)),
-           "fa_bwd_strided")
+                              scale, int(causal), mask, options, _stream(stream)),
+           "fa_bwd_fp32_ex")
 
 
-def fa_bwd_fp32_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
-                        scale, causal, mask=None, layouts=None, stream=None):
-    _check(lib.fa_bwd_fp32_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dO), _ptr(lse),
-                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                                   workspace_bytes, B, H, N, d, scale, int(causal), mask, layouts,
-                                   _stream(stream)), "fa_bwd_fp32_strided")
+def fa_bwd_preprocess_ex(o, dO, D, B, H, N, d, options=None, stream=None):
+    _check(lib.fa_bwd_preprocess_ex(_ptr(o), _ptr(dO), _ptr(D), B, H, N, d, options,
+                                    _stream(stream)), "fa_bwd_preprocess_ex")
+
+
+def fa_bwd_dkdv_ex(q, k, v, dO, lse, D, dk, dv, B, H, N, d, scale, causal, mask=None,
+                   options=None, stream=None):
+    _check(lib.fa_bwd_dkdv_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dk),
+                              _ptr(dv), B, H, N, d, scale, int(causal), mask, options,
+                              _stream(stream)), "fa_bwd_dkdv_ex")
+
+
+def fa_bwd_dq_ex(q, k, v, dO, lse, D, dq, B, H, N, d, scale, causal, mask=None, options=None,
+                 stream=None):
+    _check(lib.fa_bwd_dq_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _ptr(lse), _ptr(D), _ptr(dq),
+                            B, H, N, d, scale, int(causal), mask, options, _stream(stream)),
+           "fa_bwd_dq_ex")
+
+
+def fa_debug_dropout_mask(out, B, H, N, p, seed, offset, path, stream=None):
+    """Writes the keep mask (uint8 [B*H, N, N]) through kernel path 0, 1 or 2."""
+    dr = FaDropout(p, seed, offset)
+    _check(lib.fa_debug_dropout_mask(_ptr(out), B, H, N, ctypes.byref(dr), path,
+                                     _stream(stream)), "fa_debug_dropout_mask")
 
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, stream=None):
@@ -276,24 +334,26 @@ def _shape(q, *others):
     return tuple(int(x) for x in q.shape)
 
 
-def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None):
+def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None,
+            dropout_p=0.0, seed=0, offset=0):
     """(O, lse) for CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32) of any layout
     whose last dimension is contiguous; O takes q's layout where torch can
-    keep it (torch.empty_like)."""
+    keep it (torch.empty_like).  dropout_p > 0 drops attention probabilities
+    (bf16 only); the backward needs the same dropout_p, seed and offset."""
     import torch
     B, H, N, d = _shape(q, k, v)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     mask = make_mask(kv_len, block_mask)
-    layouts = make_layouts(q=q, k=k, v=v, o=o)
-    fn = fa_fwd_strided if q.dtype == torch.bfloat16 else fa_fwd_fp32_strided
-    fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, stream)
+    opt = make_options(make_layouts(q=q, k=k, v=v, o=o), dropout_p, seed, offset)
+    fn = fa_fwd_ex if q.dtype == torch.bfloat16 else fa_fwd_fp32_ex
+    fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, opt, stream)
     return o, lse
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_mask=None,
-             stream=None, workspace=None):
+             stream=None, workspace=None, dropout_p=0.0, seed=0, offset=0):
     """(dQ, dK, dV) for the forward above and output gradient do; each
     gradient takes the layout of its input where torch can keep it."""
     import torch
@@ -305,7 +365,8 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_m
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     mask = make_mask(kv_len, block_mask)
     layouts = make_layouts(q=q, k=k, v=v, o=o, dO=do, dq=dq, dk=dk, dv=dv)
-    fn = fa_bwd_strided if q.dtype == torch.bfloat16 else fa_bwd_fp32_strided
+    opt = make_options(layouts, dropout_p, seed, offset)
+    fn = fa_bwd_ex if q.dtype == torch.bfloat16 else fa_bwd_fp32_ex
     fn(q, k, v, o, do, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, mask,
-       layouts, stream)
+       opt, stream)
     return dq, dk, dv

@@ -101,6 +101,27 @@ fa_status check_layout(const fa_layout* in, int B, int H, int N, int d, int esiz
   return FA_OK;
 }
 
+// Validates a dropout request and derives the kernels' parameters: the
+// 16-bit threshold t = min(65535, floor(p 65536 + 1/2)) (keep probability
+// 1 - t/65536 exactly) and the scale 65536 / (65536 - t).  No request, or
+// t = 0, is no dropout.
+fa_status check_dropout(const fa_dropout* dr, int esize, DropParams* out) {
+  *out = DropParams{0u, 0u, 0u, 0u, 1.f};
+  if (!dr) return FA_OK;
+  const float p = dr->p;
+  if (!(p >= 0.f && p < 1.f)) return FA_ERR_INVALID_ARG;  // NaN fails too
+  const double tt = floor((double)p * 65536.0 + 0.5);
+  const uint32_t t = tt > 65535.0 ? 65535u : (uint32_t)tt;
+  if (t == 0) return FA_OK;
+  if (esize != 2) return FA_ERR_UNSUPPORTED;
+  out->t = t;
+  out->k0 = (uint32_t)(dr->seed & 0xFFFFFFFFull);
+  out->k1 = (uint32_t)(dr->seed >> 32);
+  out->offset = dr->offset;
+  out->rp = (float)(65536.0 / (65536.0 - (double)t));
+  return FA_OK;
+}
+
 }  // namespace
 
 bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B, int H, int N,
@@ -145,9 +166,11 @@ static bool attach_status(Args* a) {
 
 static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* v, void* o,
                           float* lse, int B, int H, int N, int d, float scale, int causal,
-                          const fa_mask* mask, const fa_layouts* L, int esize) {
+                          const fa_mask* mask, const fa_options* opt, int esize) {
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  const fa_layouts* L = opt ? opt->layouts : nullptr;
+  if ((st = check_dropout(opt ? opt->dropout : nullptr, esize, &a->drop)) != FA_OK) return st;
   if ((st = check_layout(L ? &L->q : nullptr, B, H, N, d, esize, &a->lq)) != FA_OK ||
       (st = check_layout(L ? &L->k : nullptr, B, H, N, d, esize, &a->lk)) != FA_OK ||
       (st = check_layout(L ? &L->v : nullptr, B, H, N, d, esize, &a->lv)) != FA_OK ||
@@ -168,10 +191,12 @@ static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* 
 }
 
 static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float scale, int causal,
-                                 const fa_mask* mask, const fa_layouts* L = nullptr,
+                                 const fa_mask* mask, const fa_options* opt = nullptr,
                                  int esize = 2) {
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
+  const fa_layouts* L = opt ? opt->layouts : nullptr;
+  if ((st = check_dropout(opt ? opt->dropout : nullptr, esize, &a->drop)) != FA_OK) return st;
   const fa_layout* in[8] = {L ? &L->q : nullptr,  L ? &L->k : nullptr,  L ? &L->v : nullptr,
                             L ? &L->o : nullptr,  L ? &L->dO : nullptr, L ? &L->dq : nullptr,
                             L ? &L->dk : nullptr, L ? &L->dv : nullptr};
@@ -201,8 +226,8 @@ static fa_status fill_bwd_full(BwdArgs* a, const void* q, const void* k, const v
                                const void* o, const void* dO, const float* lse, void* dq,
                                void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
                                int H, int N, int d, float scale, int causal, const fa_mask* mask,
-                               const fa_layouts* layouts, int esize) {
-  fa_status st = fill_bwd_common(a, B, H, N, d, scale, causal, mask, layouts, esize);
+                               const fa_options* opt, int esize) {
+  fa_status st = fill_bwd_common(a, B, H, N, d, scale, causal, mask, opt, esize);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
@@ -246,14 +271,14 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int d, float scale, int causal, const fa_mask* mask, void* stream) {
-  return fa_fwd_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
+  return fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
 }
 
-fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                         int H, int N, int d, float scale, int causal, const fa_mask* mask,
-                         const fa_layouts* layouts, void* stream) {
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int N, int d, float scale, int causal, const fa_mask* mask,
+                    const fa_options* options, void* stream) {
   FwdArgs a{};
-  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, 2);
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, options, 2);
   if (st != FA_OK) return st;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_fwd_bf16(a, static_cast<cudaStream_t>(stream)));
@@ -262,14 +287,14 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
 fa_status fa_fwd_fp32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
                       int H, int N, int d, float scale, int causal, const fa_mask* mask,
                       void* stream) {
-  return fa_fwd_fp32_strided(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
+  return fa_fwd_fp32_ex(q, k, v, o, lse, B, H, N, d, scale, causal, mask, nullptr, stream);
 }
 
-fa_status fa_fwd_fp32_strided(const float* q, const float* k, const float* v, float* o, float* lse,
-                              int B, int H, int N, int d, float scale, int causal,
-                              const fa_mask* mask, const fa_layouts* layouts, void* stream) {
+fa_status fa_fwd_fp32_ex(const float* q, const float* k, const float* v, float* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_options* options, void* stream) {
   FwdArgs a{};
-  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, layouts, 4);
+  fa_status st = fill_fwd(&a, q, k, v, o, lse, B, H, N, d, scale, causal, mask, options, 4);
   if (st != FA_OK) return st;
   if (!attach_status(&a)) return FA_ERR_CUDA;
   return launched(launch_fwd_fp32(a, static_cast<cudaStream_t>(stream)));
@@ -279,18 +304,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
                  size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
                  const fa_mask* mask, void* stream) {
-  return fa_bwd_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
-                        scale, causal, mask, nullptr, stream);
+  return fa_bwd_ex(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
+                   causal, mask, nullptr, stream);
 }
 
-fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
-                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
-                         void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                         float scale, int causal, const fa_mask* mask, const fa_layouts* layouts,
-                         void* stream) {
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                    const fa_mask* mask, const fa_options* options, void* stream) {
   BwdArgs a{};
   fa_status st = fill_bwd_full(&a, q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B,
-                               H, N, d, scale, causal, mask, layouts, 2);
+                               H, N, d, scale, causal, mask, options, 2);
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launched(launch_bwd_preprocess(a, s));
@@ -301,8 +325,13 @@ fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void
 
 fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, int B, int H, int N, int d,
                             void* stream) {
+  return fa_bwd_preprocess_ex(o, dO, D, B, H, N, d, nullptr, stream);
+}
+
+fa_status fa_bwd_preprocess_ex(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                               const fa_options* options, void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr);
+  fa_status st = fill_bwd_common(&a, B, H, N, d, 1.0f, 0, nullptr, options);
   if (st != FA_OK) return st;
   if (!o || !dO || !D) return FA_ERR_INVALID_ARG;
   if (!aligned16(o) || !aligned16(dO) || !aligned4(D)) return FA_ERR_ALIGNMENT;
@@ -314,8 +343,16 @@ fa_status fa_bwd_preprocess(const void* o, const void* dO, float* D, int B, int 
 fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* dO,
                       const float* lse, const float* D, void* dk, void* dv, int B, int H, int N,
                       int d, float scale, int causal, const fa_mask* mask, void* stream) {
+  return fa_bwd_dkdv_ex(q, k, v, dO, lse, D, dk, dv, B, H, N, d, scale, causal, mask, nullptr,
+                        stream);
+}
+
+fa_status fa_bwd_dkdv_ex(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, void* dk, void* dv, int B, int H,
+                         int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_options* options, void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask, options);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !dO || !lse || !D || !dk || !dv) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
@@ -330,8 +367,15 @@ fa_status fa_bwd_dkdv(const void* q, const void* k, const void* v, const void* d
 fa_status fa_bwd_dq(const void* q, const void* k, const void* v, const void* dO, const float* lse,
                     const float* D, void* dq, int B, int H, int N, int d, float scale, int causal,
                     const fa_mask* mask, void* stream) {
+  return fa_bwd_dq_ex(q, k, v, dO, lse, D, dq, B, H, N, d, scale, causal, mask, nullptr, stream);
+}
+
+fa_status fa_bwd_dq_ex(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, void* dq, int B, int H, int N, int d,
+                       float scale, int causal, const fa_mask* mask, const fa_options* options,
+                       void* stream) {
   BwdArgs a{};
-  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask, options);
   if (st != FA_OK) return st;
   if (!q || !k || !v || !dO || !lse || !D || !dq) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned4(lse) ||
@@ -347,18 +391,18 @@ fa_status fa_bwd_fp32(const float* q, const float* k, const float* v, const floa
                       const float* dO, const float* lse, float* dq, float* dk, float* dv,
                       void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
                       float scale, int causal, const fa_mask* mask, void* stream) {
-  return fa_bwd_fp32_strided(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N,
-                             d, scale, causal, mask, nullptr, stream);
+  return fa_bwd_fp32_ex(q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d,
+                        scale, causal, mask, nullptr, stream);
 }
 
-fa_status fa_bwd_fp32_strided(const float* q, const float* k, const float* v, const float* o,
-                              const float* dO, const float* lse, float* dq, float* dk, float* dv,
-                              void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                              float scale, int causal, const fa_mask* mask,
-                              const fa_layouts* layouts, void* stream) {
+fa_status fa_bwd_fp32_ex(const float* q, const float* k, const float* v, const float* o,
+                         const float* dO, const float* lse, float* dq, float* dk, float* dv,
+                         void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                         float scale, int causal, const fa_mask* mask, const fa_options* options,
+                         void* stream) {
   BwdArgs a{};
   fa_status st = fill_bwd_full(&a, q, k, v, o, dO, lse, dq, dk, dv, workspace, workspace_bytes, B,
-                               H, N, d, scale, causal, mask, layouts, 4);
+                               H, N, d, scale, causal, mask, options, 4);
   if (st != FA_OK) return st;
   return launched(launch_bwd_fp32(a, static_cast<cudaStream_t>(stream)));
 }
@@ -394,6 +438,18 @@ fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int 
   if (!st) return FA_ERR_CUDA;
   return launched(launch_umma_probe(a, b, d, M, N, K, a_mn_major, b_mn_major, a_in_tmem, use_tma,
                                     st, static_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_dropout* dropout,
+                                int path, void* stream) {
+  if (!out || !dropout) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
+  if (N > 4096) return FA_ERR_UNSUPPORTED;
+  if (path < 0 || path > 2) return FA_ERR_INVALID_ARG;
+  DropParams d;
+  const fa_status st = check_dropout(dropout, 2, &d);
+  if (st != FA_OK) return st;
+  return launched(launch_dropout_mask(out, B * H, N, d, path, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {

@@ -55,6 +55,7 @@ struct DqParams {
   const float* Dvec;
   __nv_bfloat16* dq;
   Layout ldq;
+  DropParams drop;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -72,7 +73,7 @@ struct KTileIter {
   __device__ int next(int j) const { return bits ? next_tile_bit(bits, j, jend) : j; }
 };
 
-template <int D>
+template <int D, bool kDrop>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -282,12 +283,14 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       const int x = u & 1;  // dP buffer
       const uint32_t tS = tmem + C::kColS + lane_off + col0;
       const uint32_t tP = tmem + C::kColDP + 128 * x + lane_off + col0;
-      ok = mbar_wait_warp(&s_full, u & 1, &abort_flag, p.status, 901);
-      if (!ok) break;
-      tc_fence_after();
       // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
       // causal, key <= q
       const int key0 = j * 128 + col0;
+      // dropout: keep bits of the 32 keys, drawn while S is computed
+      const uint32_t keep = kDrop ? keep_bits_of_row(p.drop, (uint32_t)bh, q, key0) : 0u;
+      ok = mbar_wait_warp(&s_full, u & 1, &abort_flag, p.status, 901);
+      if (!ok) break;
+      tc_fence_after();
       int lim = kv_limit - key0;
       if (p.causal) lim = min(lim, q - key0 + 1);
       const bool partial = lim < 32;
@@ -323,7 +326,17 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const uint32_t* rp = rp_all + 16 * h;
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])), nd2);
+          const float2 dpv = make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1]));
+          float2 t;
+          if constexpr (kDrop) {
+            // dS = P o (Z o dP / (1 - p) - D): dropped entries keep only -D
+            const int c = 16 * h + e;
+            const float2 zr = make_float2(((keep >> c) & 1u) ? p.drop.rp : 0.f,
+                                          ((keep >> (c + 1)) & 1u) ? p.drop.rp : 0.f);
+            t = fma2(dpv, zr, nd2);
+          } else {
+            t = add2(dpv, nd2);
+          }
           const float2 dsv = mul2(mul2(make_float2(pf[16 * h + e], pf[16 * h + e + 1]), sc2), t);
           dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
         }
@@ -403,10 +416,12 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq_kernel<D>,
+  p.drop = a.drop;
+  auto kernel = a.drop.t ? fa_bwd_dq_kernel<D, true> : fa_bwd_dq_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
+  kernel<<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 

@@ -63,6 +63,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   Layout ldk, ldv;
+  DropParams drop;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -80,19 +81,22 @@ struct QTileIter {
   __device__ int next(int i) const { return bits ? next_tile_bit(bits, i, T) : i; }
 };
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, int n) {
+// n fp32 values (TMEM words) times `mult`, stored as bf16.
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_t* r, int n,
+                                               float mult) {
   uint4* d4 = reinterpret_cast<uint4*>(dst);
+  auto f = [&](int e) { return __uint_as_float(r[e]) * mult; };
   for (int g = 0; g < n / 8; ++g) {
     uint4 w;
-    w.x = pack_bf16(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1]));
-    w.y = pack_bf16(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3]));
-    w.z = pack_bf16(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5]));
-    w.w = pack_bf16(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7]));
+    w.x = pack_bf16(f(8 * g), f(8 * g + 1));
+    w.y = pack_bf16(f(8 * g + 2), f(8 * g + 3));
+    w.z = pack_bf16(f(8 * g + 4), f(8 * g + 5));
+    w.w = pack_bf16(f(8 * g + 6), f(8 * g + 7));
     d4[g] = w;
   }
 }
 
-template <int D>
+template <int D, bool kDrop>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -338,6 +342,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // thread is past this tile's dS (the loads' latency hides behind the MMAs)
       RowStats next_st{};
       if (tid < 128) next_st = load_stats(qtiles.next(i + 1));
+      // dropout: keep bits of this key for the warpgroup's 32 query rows,
+      // drawn while S^T is computed
+      const uint32_t keep =
+          kDrop ? keep_bits_of_key(p.drop, (uint32_t)bh, key, i * 128 + col0) : 0u;
       ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
       if (ok) ok = mbar_wait_warp(&s_ready, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
@@ -373,7 +381,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         uint32_t pp[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) pp[e / 2] = pack_bf16(pf[16 * h + e], pf[16 * h + e + 1]);
+        for (int e = 0; e < 16; e += 2) {
+          float a0 = pf[16 * h + e], a1 = pf[16 * h + e + 1];
+          if constexpr (kDrop) {  // dV takes (P o Z)^T; the 1 / (1 - p) is applied at the end
+            if (!((keep >> (16 * h + e)) & 1u)) a0 = 0.f;
+            if (!((keep >> (16 * h + e + 1)) & 1u)) a1 = 0.f;
+          }
+          pp[e / 2] = pack_bf16(a0, a1);
+        }
         FA_TMEM_ST8(tmem + C::kColS + lane_off + col0 + 8 * h, pp);
       }
       tmem_wait_st();
@@ -397,8 +412,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 4 * g + 2 * u;
-            const float2 t = add2(make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1])),
-                                  u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y));
+            const float2 dpv = make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1]));
+            const float2 nD = u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y);
+            float2 t;
+            if constexpr (kDrop) {
+              // dS^T = P^T o (Z o dP^T / (1 - p) - D): dropped entries keep only -D
+              const int c = 16 * h + e;
+              const float2 zr = make_float2(((keep >> c) & 1u) ? p.drop.rp : 0.f,
+                                            ((keep >> (c + 1)) & 1u) ? p.drop.rp : 0.f);
+              t = fma2(dpv, zr, nD);
+            } else {
+              t = add2(dpv, nD);
+            }
             const float2 dsv = mul2(mul2(make_float2(pf[16 * h + e], pf[16 * h + e + 1]), sc2), t);
             dsp[8 * h + e / 2] = pack_bf16(dsv.x, dsv.y);
           }
@@ -444,7 +469,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           for (int e = 0; e < C::kDSlice; ++e) rr[e] = 0u;
         }
         if (key < p.N)
-          store_row_bf16(which == 0 ? p.dv + base_v : p.dk + base_k, rr, C::kDSlice);
+          store_row_bf16(which == 0 ? p.dv + base_v : p.dk + base_k, rr, C::kDSlice,
+                         (kDrop && which == 0) ? p.drop.rp : 1.f);
       }
     }
   }
@@ -475,6 +501,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   p.dv = static_cast<__nv_bfloat16*>(a.dv);
   p.ldk = a.ldk;
   p.ldv = a.ldv;
+  p.drop = a.drop;
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
   p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
   p.H = a.H;
@@ -485,10 +512,11 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(fa_bwd_dkdv_kernel<D>,
+  auto kernel = a.drop.t ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dkdv_kernel<D><<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
+  kernel<<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 

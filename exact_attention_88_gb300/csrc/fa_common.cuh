@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fa_internal.h"
+
 namespace fa {
 
 // ---------------------------------------------------------------------------
@@ -162,6 +164,98 @@ __device__ __forceinline__ int next_tile_bit(const uint32_t* bits, int t, int en
     t = (t | 31) + 1;
   }
   return end;
+}
+
+// ---------------------------------------------------------------------------
+// Dropout: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random
+// numbers: as easy as 1, 2, 3", SC 2011), from its published definition: ten
+// rounds; each multiplies counter words 0 and 2 by M0 = 0xD2511F53 and
+// M1 = 0xCD9E8D57 (64-bit products) and maps (c0, c1, c2, c3) to
+// (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key
+// is bumped by the Weyl constants W0 = 0x9E3779B9, W1 = 0xBB67AE85 between
+// rounds.
+//
+// Element (i, j) of head bh uses the call with counter (j / 8, i, bh, offset);
+// its four output words hold eight 16-bit uniforms, key j taking the low
+// (j even) or high (j odd) half of word (j % 8) / 2, and the element is kept
+// when that uniform is >= t.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                               uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = c0 * 0xD2511F53u, hi0 = __umulhi(c0, 0xD2511F53u);
+    const uint32_t lo1 = c2 * 0xCD9E8D57u, hi1 = __umulhi(c2, 0xCD9E8D57u);
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// Per-halfword keep masks of one output word: 0xFFFF where the uniform >= t.
+__device__ __forceinline__ uint32_t keep_halves(uint32_t w, uint32_t t) {
+  return __vcmpgeu2(w, t | (t << 16));
+}
+
+// The keep bits (bit m: key 8g + m) of one call's eight uniforms.
+__device__ __forceinline__ uint32_t keep_bits8(uint4 w, uint32_t t) {
+  const uint32_t x01 = __byte_perm(keep_halves(w.x, t), keep_halves(w.y, t), 0x6420);
+  const uint32_t x23 = __byte_perm(keep_halves(w.z, t), keep_halves(w.w, t), 0x6420);
+  // byte k of x01 / x23 is 0xFF when key k / 4 + k is kept: keep one bit per
+  // byte, then add the four bytes into the top byte (no carries: distinct bits)
+  const uint32_t lo = ((x01 & 0x08040201u) * 0x01010101u) >> 24;
+  const uint32_t hi = ((x23 & 0x80402010u) * 0x01010101u) >> 24;
+  return lo | hi;
+}
+
+// Keep masks of keys 8g .. 8g+7 of query row i: word p holds keys 2p (low
+// half) and 2p + 1 (high half), 0xFFFF where kept -- an AND mask for packed
+// bf16 pairs (the forward and dQ kernels: a query row per thread).
+__device__ __forceinline__ uint4 keep_group(const DropParams& d, uint32_t bh, int i, int g) {
+  const uint4 w = philox4x32_10((uint32_t)g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
+  return make_uint4(keep_halves(w.x, d.t), keep_halves(w.y, d.t), keep_halves(w.z, d.t),
+                    keep_halves(w.w, d.t));
+}
+
+// Keep bits of keys key0 + c, c = 0..31 (bit c), of query row i; key0 is a
+// multiple of 8 (the dQ kernel: a query row per thread, 32 keys at a time).
+__device__ __forceinline__ uint32_t keep_bits_of_row(const DropParams& d, uint32_t bh, int i,
+                                                     int key0) {
+  uint32_t bits = 0;
+#pragma unroll 1
+  for (int g = 0; g < 4; ++g) {  // one call at a time: few registers
+    const uint4 w = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
+    bits |= keep_bits8(w, d.t) << (8 * g);
+  }
+  return bits;
+}
+
+// Keep bits of query rows q0 + c, c = 0..31 (bit c), for this lane's key (the
+// dK/dV kernel: a key per thread).  The eight lanes of each aligned group of
+// eight hold eight consecutive keys (key % 8 == lane % 8), and all 32 lanes
+// take part: lane L draws the calls of rows q0 + L + 8r (r = 0..3), which
+// cover the group's eight keys, and the lanes swap the bits through shuffles.
+__device__ __forceinline__ uint32_t keep_bits_of_key(const DropParams& d, uint32_t bh, int key,
+                                                     int q0) {
+  const int lane = threadIdx.x & 31, m = key & 7;
+  uint32_t mine = 0;  // byte r: the group's keys for row q0 + (lane % 8) + 8r
+#pragma unroll 1
+  for (int r = 0; r < 4; ++r) {  // one call at a time: few registers
+    const uint4 w = philox4x32_10((uint32_t)key >> 3, (uint32_t)(q0 + (lane & 7) + 8 * r), bh,
+                                  d.offset, d.k0, d.k1);
+    mine |= keep_bits8(w, d.t) << (8 * r);
+  }
+  uint32_t out = 0;
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint32_t k = __shfl_sync(0xffffffffu, mine, (lane & ~7) | s);
+    out |= ((k >> m) & 0x01010101u) << s;  // rows s + 8r -> bits s + 8r
+  }
+  return out;
 }
 
 // One arrival for the whole warp, made by lane 0 once every lane has got

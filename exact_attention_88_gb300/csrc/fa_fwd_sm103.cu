@@ -52,6 +52,7 @@ struct FwdCfg {
 struct FwdParams {
   __nv_bfloat16* o;
   Layout lo;
+  DropParams drop;
   float* lse;
   const int32_t* kv_len;
   const uint8_t* block_mask;
@@ -105,9 +106,11 @@ __device__ __forceinline__ float max64(const uint32_t* r) {
   return fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7]));
 }
 
+template <bool kDrop>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
-                                             bool first, float& m, float& l, uint64_t* p_half) {
+                                             bool first, float& m, float& l, uint64_t* p_half,
+                                             const DropParams& drop, uint32_t bh) {
   // keys [0, lim) of the tile are visible from this row
   int lim = kv_limit - key0;
   if (causal) lim = min(lim, row - key0 + 1);
@@ -153,12 +156,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     FA_TMEM_LD64_SYNC(tS + 64 * half, r);
     if (partial) mask_tail(r, lim - 64 * half);
     uint32_t pk[32];
+    uint4 keep;  // dropout: keep masks of the current group of eight keys
 #pragma unroll
     for (int e = 0; e < 64; e += 2) {
       const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
       const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-      acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);
-      pk[e >> 1] = pack_bf16(pv.x, pv.y);
+      acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);  // l sums the undropped P~
+      uint32_t pair = pack_bf16(pv.x, pv.y);
+      if constexpr (kDrop) {
+        if ((e & 7) == 0) keep = keep_group(drop, bh, row, (key0 >> 3) + 8 * half + (e >> 3));
+        const int w = (e >> 1) & 3;
+        pair &= w == 0 ? keep.x : w == 1 ? keep.y : w == 2 ? keep.z : keep.w;
+      }
+      pk[e >> 1] = pair;
     }
     // packed P of keys [64 half, 64 half + 64) over S columns [32 half, 32 half + 32),
     // which this thread has already read
@@ -178,7 +188,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
   tmem_wait_st();
 }
 
-template <int D>
+template <int D, bool kDrop>
 __global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -382,8 +392,8 @@ __global__ void __launch_bounds__(352, 1)
           ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
           if (!ok) break;
           tc_fence_after();
-          softmax_tile(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0, p.scale_log2, n == 0,
-                       m, l, &p_half[x]);
+          softmax_tile<kDrop>(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0,
+                              p.scale_log2, n == 0, m, l, &p_half[x], p.drop, (uint32_t)bh);
           tc_fence_before();
           mbar_arrive_warp(&p_full[x]);
           ++n;
@@ -400,7 +410,8 @@ __global__ void __launch_bounds__(352, 1)
       }
       if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
         const bool empty_row = !(l > 0.f);
-        const float inv = empty_row ? 0.f : 1.f / l;
+        // dropout: the kept entries of P are scaled by 1 / (1 - p)
+        const float inv = empty_row ? 0.f : (kDrop ? p.drop.rp : 1.f) / l;
         const long long base = row_offset(p.lo, b, hd, row);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -463,11 +474,12 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
-  cudaError_t e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmem);
+  p.drop = a.drop;
+  auto kernel = a.drop.t ? fa_fwd_kernel<D, true> : fa_fwd_kernel<D, false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.pairs * BH);
-  fa_fwd_kernel<D><<<grid, C::kThreads, C::kSmem, s>>>(mq, mk, mv, p);
+  kernel<<<grid, C::kThreads, C::kSmem, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 

@@ -38,6 +38,15 @@ __host__ __device__ inline long long row_offset(const Layout& l, int b, int h, i
   return (long long)b * l.b + (long long)h * l.h + (long long)n * l.n;
 }
 
+// Dropout of one launch (the generator and the counter layout are described
+// with philox4x32_10 in fa_common.cuh).
+struct DropParams {
+  uint32_t t;       // 16-bit drop threshold; 0: no dropout
+  uint32_t k0, k1;  // key: seed low, seed high
+  uint32_t offset;  // fourth counter word
+  float rp;         // 65536 / (65536 - t): scale of the kept probabilities
+};
+
 // Everything a forward launch needs.  Pointers are device pointers.
 struct FwdArgs {
   const void* q;
@@ -46,6 +55,7 @@ struct FwdArgs {
   void* o;
   float* lse;  // dense fp32 [B,H,N]
   Layout lq, lk, lv, lo;
+  DropParams drop;
   int B, H, N, d;
   float scale;
   int causal;
@@ -67,6 +77,7 @@ struct BwdArgs {
   void* dk;
   void* dv;
   Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
+  DropParams drop;
   int B, H, N, d;
   float scale;
   int causal;
@@ -98,6 +109,8 @@ cudaError_t launch_umma_probe(const void* a, const void* b, float* d, int M, int
                               int a_mn, int b_mn, int a_tmem, int use_tma, int* status,
                               cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
+cudaError_t launch_dropout_mask(uint8_t* out, int BH, int N, const DropParams& d, int path,
+                                cudaStream_t s);
 
 inline int tiles_of(int n, int t) { return (n + t - 1) / t; }
 

@@ -181,4 +181,59 @@ cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStre
   return cudaGetLastError();
 }
 
+namespace {
+
+// Dropout keep mask out[bh][i][j] through the row path of the forward and dQ
+// kernels: a thread per (bh, row i, group of eight keys g).
+__global__ void dropout_mask_rows_kernel(uint8_t* out, int N, DropParams d) {
+  const int bh = blockIdx.z, i = blockIdx.y;
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (8 * g >= N) return;
+  const uint4 m = keep_group(d, (uint32_t)bh, i, g);
+  const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+  uint8_t* row = out + ((size_t)bh * N + i) * N;
+#pragma unroll
+  for (int e = 0; e < 8; ++e)
+    if (8 * g + e < N) row[8 * g + e] = (uint8_t)((w[e >> 1] >> (16 * (e & 1))) & 1u);
+}
+
+// The same through the row path of the dQ kernel: a thread per (bh, row i,
+// 32 keys).
+__global__ void dropout_mask_rowbits_kernel(uint8_t* out, int N, DropParams d) {
+  const int bh = blockIdx.z, i = blockIdx.y;
+  const int key0 = 32 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (key0 >= N) return;
+  const uint32_t bits = keep_bits_of_row(d, (uint32_t)bh, i, key0);
+  uint8_t* row = out + ((size_t)bh * N + i) * N;
+  for (int c = 0; c < 32 && key0 + c < N; ++c) row[key0 + c] = (uint8_t)((bits >> c) & 1u);
+}
+
+// The same through the key path of the dK/dV kernel: each warp takes 32
+// consecutive keys (a key per lane) and 32 query rows; every lane takes part
+// in the shuffles, only entries inside [0, N) are written.
+__global__ void dropout_mask_keys_kernel(uint8_t* out, int N, DropParams d) {
+  const int bh = blockIdx.z, q0 = 32 * blockIdx.y;
+  const int key = 32 * (4 * blockIdx.x + (threadIdx.x >> 5)) + (threadIdx.x & 31);
+  const uint32_t bits = keep_bits_of_key(d, (uint32_t)bh, key, q0);
+  if (key >= N) return;
+  for (int c = 0; c < 32 && q0 + c < N; ++c)
+    out[((size_t)bh * N + q0 + c) * N + key] = (uint8_t)((bits >> c) & 1u);
+}
+
+}  // namespace
+
+cudaError_t launch_dropout_mask(uint8_t* out, int BH, int N, const DropParams& d, int path,
+                                cudaStream_t s) {
+  if (path == 0) {
+    const int groups = (N + 7) / 8;
+    dropout_mask_rows_kernel<<<dim3((groups + 127) / 128, N, BH), 128, 0, s>>>(out, N, d);
+  } else if (path == 2) {
+    const int chunks = (N + 31) / 32;
+    dropout_mask_rowbits_kernel<<<dim3((chunks + 127) / 128, N, BH), 128, 0, s>>>(out, N, d);
+  } else {
+    dropout_mask_keys_kernel<<<dim3((N + 127) / 128, (N + 31) / 32, BH), 128, 0, s>>>(out, N, d);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace fa

@@ -20,9 +20,10 @@
  *
  * Conventions shared by every call:
  *   - Tensors are dense row-major [B, H, N, d] (d contiguous) in DEVICE
- *     memory, 16-byte aligned; lse and D are fp32 [B, H, N].  The *_strided
+ *     memory, 16-byte aligned; lse and D are fp32 [B, H, N].  The *_ex
  *     calls take Q, K, V, O, dO, dQ, dK, dV in any layout whose d elements of
- *     a row are contiguous (fa_layout); lse and D stay dense.  The caller owns
+ *     a row are contiguous (fa_layout), and dropout (fa_dropout); lse and D
+ *     stay dense.  The caller owns
  *     every buffer; the library allocates nothing.
  *   - bf16 calls take bf16 (uint16 storage) Q, K, V, O, dO, dQ, dK, dV and
  *     accumulate in fp32.  *_fp32 calls take fp32 everywhere.
@@ -157,27 +158,69 @@ typedef struct {
   fa_layout q, k, v, o, dO, dq, dk, dv;
 } fa_layouts;
 
-/* fa_fwd / fa_bwd / fa_fwd_fp32 / fa_bwd_fp32 with a layout per tensor
- * (NULL = every tensor dense); every other argument as in the dense call.
- * The work and the results are those of the dense call on the same values:
- * the kernels read and write through the strides (the TMA descriptors of the
- * bf16 kernels carry them), nothing is copied. */
-fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                         int H, int N, int d, float scale, int causal, const fa_mask* mask,
-                         const fa_layouts* layouts, void* stream);
-fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o,
-                         const void* dO, const float* lse, void* dq, void* dk, void* dv,
+/* Dropout on the attention probabilities.  The summary page lists dropout
+ * among the operations fused into the attention kernel and says that the
+ * backward pass keeps the generator's state to regenerate the mask on chip
+ * ("Key ideas: kernel fusion"; its question on the auxiliary memory of the
+ * backward pass).  Reading: with Z_ij in {0, 1} kept with probability 1 - p,
+ *     O = (P o Z) V / (1 - p),   lse of the undropped scores,
+ * and the backward is the chain rule through it (dV = (P o Z)^T dO / (1-p),
+ * dS = P o (Z o dO V^T / (1-p) - D), D = rowsum(dO o O) as without dropout).
+ * Z is drawn from Philox4x32-10 (Salmon et al., "Parallel random numbers: as
+ * easy as 1, 2, 3", SC 2011): element (i, j) of head (b, h) takes the call
+ * with counter (j / 8, i, b*H + h, offset) and key (seed & 0xFFFFFFFF,
+ * seed >> 32); of its four output words, key j takes the low (j even) or
+ * high (j odd) 16 bits of word (j % 8) / 2 and is kept when they are >= t,
+ * t = min(65535, floor(p * 65536 + 0.5)) -- so the keep probability is
+ * exactly 1 - t/65536 and the kept entries are scaled by 65536 / (65536 - t).
+ * The forward and backward of one step must use the same p, seed, offset. */
+typedef struct {
+  float p;          /* drop probability, 0 <= p < 1 (0: no dropout)          */
+  uint64_t seed;    /* generator key                                         */
+  uint32_t offset;  /* fourth counter word: a new value per step (e.g. the step number) */
+} fa_dropout;
+
+/* Options of the *_ex calls.  NULL options, or NULL members, mean dense
+ * tensors and no dropout. */
+typedef struct {
+  const fa_layouts* layouts;
+  const fa_dropout* dropout;  /* bf16 calls only: FA_ERR_UNSUPPORTED for fp32 */
+} fa_options;
+
+/* fa_fwd / fa_bwd / fa_fwd_fp32 / fa_bwd_fp32 and the three backward steps
+ * with options; every other argument as in the plain call.  With dense
+ * layouts and no dropout the work and results are those of the plain call;
+ * other layouts give the same results on the same values (the kernels read
+ * and write through the strides -- the TMA descriptors of the bf16 kernels
+ * carry them -- and nothing is copied).  Errors: a p outside [0, 1)
+ * (or NaN) is FA_ERR_INVALID_ARG; dropout on an fp32 call, FA_ERR_UNSUPPORTED. */
+fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int N, int d, float scale, int causal, const fa_mask* mask,
+                    const fa_options* options, void* stream);
+fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                    const fa_mask* mask, const fa_options* options, void* stream);
+fa_status fa_fwd_fp32_ex(const float* q, const float* k, const float* v, float* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_options* options, void* stream);
+fa_status fa_bwd_fp32_ex(const float* q, const float* k, const float* v, const float* o,
+                         const float* dO, const float* lse, float* dq, float* dk, float* dv,
                          void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                         float scale, int causal, const fa_mask* mask, const fa_layouts* layouts,
+                         float scale, int causal, const fa_mask* mask, const fa_options* options,
                          void* stream);
-fa_status fa_fwd_fp32_strided(const float* q, const float* k, const float* v, float* o, float* lse,
-                              int B, int H, int N, int d, float scale, int causal,
-                              const fa_mask* mask, const fa_layouts* layouts, void* stream);
-fa_status fa_bwd_fp32_strided(const float* q, const float* k, const float* v, const float* o,
-                              const float* dO, const float* lse, float* dq, float* dk, float* dv,
-                              void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
-                              float scale, int causal, const fa_mask* mask,
-                              const fa_layouts* layouts, void* stream);
+/* The backward steps with options (layouts of o, dO for the preprocess;
+ * dropout for fa_bwd_dkdv_ex and fa_bwd_dq_ex). */
+fa_status fa_bwd_preprocess_ex(const void* o, const void* dO, float* D, int B, int H, int N, int d,
+                               const fa_options* options, void* stream);
+fa_status fa_bwd_dkdv_ex(const void* q, const void* k, const void* v, const void* dO,
+                         const float* lse, const float* D, void* dk, void* dv, int B, int H,
+                         int N, int d, float scale, int causal, const fa_mask* mask,
+                         const fa_options* options, void* stream);
+fa_status fa_bwd_dq_ex(const void* q, const void* k, const void* v, const void* dO,
+                       const float* lse, const float* D, void* dq, int B, int H, int N, int d,
+                       float scale, int causal, const fa_mask* mask, const fa_options* options,
+                       void* stream);
 
 /* Size of the fixed scratch array fa_bwd_noalloc works in: 32 MiB. */
 #define FA_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -233,6 +276,15 @@ fa_status fa_get_device_status(void* stream, int* site);
 fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int N, int K,
                              int a_mn_major, int b_mn_major, int a_in_tmem, int use_tma,
                              void* stream);
+
+/* Diagnostic: writes the dropout keep mask Z (uint8 [B*H, N, N], 1 = kept)
+ * of `dropout` with the device code of the attention kernels: path 0 as the
+ * forward kernel draws it (a query row per thread, AND masks of bf16 pairs),
+ * path 2 as the dQ kernel does (a query row per thread, 32 keep bits), path 1
+ * as the dK/dV kernel does (a key per thread, the bits of each call shared
+ * among eight lanes).  `out` is device memory of B*H*N*N bytes; N <= 4096. */
+fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_dropout* dropout,
+                                int path, void* stream);
 
 /* Diagnostic: launches one CTA that waits on an mbarrier no one arrives on,
  * with the given limit (1..1000000 microseconds), exactly as the attention

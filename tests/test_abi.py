@@ -139,17 +139,19 @@ def test_substeps_reject_bad_arguments(fa):
     assert fa.lib.fa_debug_wait_timeout(2000000, None) == 1
 
 
-def strided(fa, fp32=False, bwd=False, B=2, H=2, N=128, d=64, **lay):
-    """Calls a *_strided entry point with fake pointers; `lay` overrides the
+def strided(fa, fp32=False, bwd=False, B=2, H=2, N=128, d=64, dropout=0.0, **lay):
+    """Calls an *_ex entry point with fake pointers; `lay` overrides the
     (batch, head, row) strides of named tensors, the rest dense."""
     ls = fa.FaLayouts()
     for name in ("q", "k", "v", "o", "dO", "dq", "dk", "dv"):
         setattr(ls, name, fa.FaLayout(*lay.get(name, (H * N * d, N * d, d))))
-    L = ctypes.pointer(ls)
+    L = fa.make_options(ls, dropout, 1, 2)
+    if dropout != dropout:   # NaN: make_options treats it as set
+        L.contents.dropout = ctypes.pointer(fa.FaDropout(dropout, 1, 2))
     if not bwd:
-        fn = fa.lib.fa_fwd_fp32_strided if fp32 else fa.lib.fa_fwd_strided
+        fn = fa.lib.fa_fwd_fp32_ex if fp32 else fa.lib.fa_fwd_ex
         return fn(FAKE, FAKE, FAKE, FAKE, FAKE, B, H, N, d, 0.125, 0, None, L, None)
-    fn = fa.lib.fa_bwd_fp32_strided if fp32 else fa.lib.fa_bwd_strided
+    fn = fa.lib.fa_bwd_fp32_ex if fp32 else fa.lib.fa_bwd_ex
     ws = fa.fa_bwd_workspace_size(B, H, N, d)
     return fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, B, H, N, d, 0.125, 0,
               None, L, None)
@@ -182,12 +184,12 @@ def test_strided_backward_needs_every_layout(fa):
     ls = fa.FaLayouts()
     for name in ("q", "k", "v", "o"):
         setattr(ls, name, fa.FaLayout(2 * 128 * 64, 128 * 64, 64))
-    L = ctypes.pointer(ls)
-    assert fa.lib.fa_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 0.125, 0, None, L,
-                                 None) == 5
+    L = fa.make_options(ls)
+    assert fa.lib.fa_fwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 128, 64, 0.125, 0, None, L,
+                            None) == 5
     ws = fa.fa_bwd_workspace_size(2, 2, 128, 64)
-    assert fa.lib.fa_bwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 2,
-                                 2, 128, 64, 0.125, 0, None, L, None) == 2
+    assert fa.lib.fa_bwd_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 2,
+                            2, 128, 64, 0.125, 0, None, L, None) == 2
 
 
 def test_layout_of_reads_torch_strides(fa):
@@ -199,3 +201,33 @@ def test_layout_of_reads_torch_strides(fa):
         fa.layout_of(torch.zeros(2, 3, 64, 5).transpose(2, 3))   # d not contiguous
     with pytest.raises(ValueError):
         fa.make_layouts(x=x)
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+def test_dropout_rules(fa, bwd):
+    assert strided(fa, bwd=bwd, dropout=0.5) == 5            # valid (no CUDA here)
+    assert strided(fa, bwd=bwd, dropout=0.999) == 5
+    assert strided(fa, bwd=bwd, dropout=1.0) == 1
+    assert strided(fa, bwd=bwd, dropout=-0.25) == 1
+    assert strided(fa, bwd=bwd, dropout=float("nan")) == 1
+    assert strided(fa, fp32=True, bwd=bwd, dropout=0.5) == 2  # fp32 path: no dropout
+    assert strided(fa, fp32=True, bwd=bwd, dropout=0.0) == 5
+    # p that rounds to a zero threshold is no dropout, also for fp32
+    assert strided(fa, fp32=True, bwd=bwd, dropout=1e-6) == 5
+    opt = fa.make_options(None, 0.5, 1, 2)
+    assert fa.lib.fa_bwd_dkdv_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64,
+                                 0.1, 0, None, opt, None) == 5
+    bad = fa.make_options(None, 0.5, 1, 2)
+    bad.contents.dropout.contents.p = 1.5
+    assert fa.lib.fa_bwd_dq_ex(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.1, 0,
+                               None, bad, None) == 1
+
+
+def test_dropout_mask_diagnostic_rejects(fa):
+    dr = ctypes.byref(fa.FaDropout(0.5, 1, 2))
+    assert fa.lib.fa_debug_dropout_mask(None, 1, 1, 64, dr, 0, None) == 1
+    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, None, 0, None) == 1
+    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 5000, dr, 0, None) == 2
+    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, dr, 3, None) == 1
+    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, ctypes.byref(fa.FaDropout(1.0, 1, 2)), 0,
+                                        None) == 1

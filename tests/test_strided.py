@@ -1,4 +1,4 @@
-"""GPU tests of the *_strided calls: the same values laid out in other
+"""GPU tests of the *_ex calls with layouts: the same values laid out in other
 layouts ([B,N,H,d], a slot of a packed QKV buffer, padded rows, heads
 outermost) must give bit for bit the results of the dense call, the outputs
 written through their own strides and nothing outside their views touched.
@@ -76,15 +76,15 @@ def run_strided(fa, t, shape, scale, causal, mask, fp32, kinds):
     for name in ("o", "dq", "dk", "dv"):
         bufs[name], views[name] = place(shape, dt, kinds[name])
     lse = torch.full((B, H, N), FILL, dtype=torch.float32, device="cuda")
-    layouts = fa.make_layouts(**views)
-    (fa.fa_fwd_fp32_strided if fp32 else fa.fa_fwd_strided)(
+    opt = fa.make_options(fa.make_layouts(**views))
+    (fa.fa_fwd_fp32_ex if fp32 else fa.fa_fwd_ex)(
         views["q"], views["k"], views["v"], views["o"], lse, B, H, N, d, scale, causal, mask,
-        layouts)
+        opt)
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    (fa.fa_bwd_fp32_strided if fp32 else fa.fa_bwd_strided)(
+    (fa.fa_bwd_fp32_ex if fp32 else fa.fa_bwd_ex)(
         views["q"], views["k"], views["v"], views["o"], views["dO"], lse, views["dq"],
-        views["dk"], views["dv"], ws, ws_bytes, B, H, N, d, scale, causal, mask, layouts)
+        views["dk"], views["dv"], ws, ws_bytes, B, H, N, d, scale, causal, mask, opt)
     torch.cuda.synchronize()
     code, site = fa.fa_get_device_status()
     assert code == 0, "device status %d at site %d" % (code, site)
@@ -184,8 +184,7 @@ def test_ignored_strides_of_size_one_dims(fa):
     ls = fa.FaLayouts()
     for name in ("q", "k", "v", "o"):
         setattr(ls, name, fa.FaLayout(0, -3, d))
-    import ctypes
-    fa.fa_fwd_strided(t["q"], t["k"], t["v"], o, lse, B, H, N, d, 0.125, True, None,
-                      ctypes.pointer(ls))
+    fa.fa_fwd_ex(t["q"], t["k"], t["v"], o, lse, B, H, N, d, 0.125, True, None,
+                 fa.make_options(ls))
     torch.cuda.synchronize()
     assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
