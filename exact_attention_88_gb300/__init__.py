@@ -237,7 +237,7 @@ def fa_bwd_dq_ex(q, k, v, dO, lse, D, dq, B, H, N, d, scale, causal, mask=None, 
 
 
 def fa_debug_dropout_mask(out, B, H, N, p, seed, offset, path, stream=None):
-    """Writes the keep mask (uint8 [B*H, N, N]) through kernel path 0, 1 or 2."""
+    """Writes the keep mask (uint8 [B*H, N, N]) through kernel path 0 (rows) or 1 (keys)."""
     dr = FaDropout(p, seed, offset)
     _check(lib.fa_debug_dropout_mask(_ptr(out), B, H, N, ctypes.byref(dr), path,
                                      _stream(stream)), "fa_debug_dropout_mask")

@@ -445,7 +445,7 @@ fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_drop
   if (!out || !dropout) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
   if (N > 4096) return FA_ERR_UNSUPPORTED;
-  if (path < 0 || path > 2) return FA_ERR_INVALID_ARG;
+  if (path != 0 && path != 1) return FA_ERR_INVALID_ARG;
   DropParams d;
   const fa_status st = check_dropout(dropout, 2, &d);
   if (st != FA_OK) return st;

@@ -184,12 +184,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
                                                uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t lo0 = c0 * 0xD2511F53u, hi0 = __umulhi(c0, 0xD2511F53u);
-    const uint32_t lo1 = c2 * 0xCD9E8D57u, hi1 = __umulhi(c2, 0xCD9E8D57u);
-    c0 = hi1 ^ c1 ^ k0;
-    c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
-    c3 = lo0;
+    const uint64_t p0 = (uint64_t)c0 * 0xD2511F53u;  // one wide multiply: both halves
+    const uint64_t p1 = (uint64_t)c2 * 0xCD9E8D57u;
+    c0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    c1 = (uint32_t)p1;
+    c2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c3 = (uint32_t)p0;
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
@@ -212,22 +212,13 @@ __device__ __forceinline__ uint32_t keep_bits8(uint4 w, uint32_t t) {
   return lo | hi;
 }
 
-// Keep masks of keys 8g .. 8g+7 of query row i: word p holds keys 2p (low
-// half) and 2p + 1 (high half), 0xFFFF where kept -- an AND mask for packed
-// bf16 pairs (the forward and dQ kernels: a query row per thread).
-__device__ __forceinline__ uint4 keep_group(const DropParams& d, uint32_t bh, int i, int g) {
-  const uint4 w = philox4x32_10((uint32_t)g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
-  return make_uint4(keep_halves(w.x, d.t), keep_halves(w.y, d.t), keep_halves(w.z, d.t),
-                    keep_halves(w.w, d.t));
-}
-
 // Keep bits of keys key0 + c, c = 0..31 (bit c), of query row i; key0 is a
-// multiple of 8 (the dQ kernel: a query row per thread, 32 keys at a time).
+// multiple of 8 (the forward and dQ kernels: a query row per thread).
 __device__ __forceinline__ uint32_t keep_bits_of_row(const DropParams& d, uint32_t bh, int i,
                                                      int key0) {
   uint32_t bits = 0;
-#pragma unroll 1
-  for (int g = 0; g < 4; ++g) {  // one call at a time: few registers
+#pragma unroll 2
+  for (int g = 0; g < 4; ++g) {  // two calls in flight: few registers
     const uint4 w = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
     bits |= keep_bits8(w, d.t) << (8 * g);
   }

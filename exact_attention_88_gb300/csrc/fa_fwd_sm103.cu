@@ -110,7 +110,7 @@ template <bool kDrop>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
                                              bool first, float& m, float& l, uint64_t* p_half,
-                                             const DropParams& drop, uint32_t bh) {
+                                             const uint32_t* kbits) {
   // keys [0, lim) of the tile are visible from this row
   int lim = kv_limit - key0;
   if (causal) lim = min(lim, row - key0 + 1);
@@ -156,19 +156,20 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     FA_TMEM_LD64_SYNC(tS + 64 * half, r);
     if (partial) mask_tail(r, lim - 64 * half);
     uint32_t pk[32];
-    uint4 keep;  // dropout: keep masks of the current group of eight keys
+    // dropout: keep bits of this half's keys [0, 32) and [32, 64)
+    const uint32_t kb0 = kDrop ? (half ? kbits[2] : kbits[0]) : 0u;
+    const uint32_t kb1 = kDrop ? (half ? kbits[3] : kbits[1]) : 0u;
 #pragma unroll
     for (int e = 0; e < 64; e += 2) {
       const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
-      const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+      float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
       acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);  // l sums the undropped P~
-      uint32_t pair = pack_bf16(pv.x, pv.y);
       if constexpr (kDrop) {
-        if ((e & 7) == 0) keep = keep_group(drop, bh, row, (key0 >> 3) + 8 * half + (e >> 3));
-        const int w = (e >> 1) & 3;
-        pair &= w == 0 ? keep.x : w == 1 ? keep.y : w == 2 ? keep.z : keep.w;
+        const uint32_t kb = e < 32 ? kb0 : kb1;
+        if (!((kb >> (e & 31)) & 1u)) pv.x = 0.f;
+        if (!((kb >> ((e + 1) & 31)) & 1u)) pv.y = 0.f;
       }
-      pk[e >> 1] = pair;
+      pk[e >> 1] = pack_bf16(pv.x, pv.y);
     }
     // packed P of keys [64 half, 64 half + 64) over S columns [32 half, 32 half + 32),
     // which this thread has already read
@@ -384,16 +385,27 @@ __global__ void __launch_bounds__(352, 1)
         // u (each turn barrier's next phase needs this warpgroup's own next
         // pass, so no waiter can fall a phase behind).  Without a tile B, A
         // runs on its own.
+        const bool vis = x == 0 ? tiles.vis_a(j) : tiles.vis_b(j);
+        // dropout: this row's keep bits of the tile, drawn before the turn and S
+        // are waited for (while the other warpgroup's softmax runs)
+        uint32_t kbits[4] = {0u, 0u, 0u, 0u};
+        if constexpr (kDrop) {
+          if (vis) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              kbits[c] = keep_bits_of_row(p.drop, (uint32_t)bh, row, j * 128 + 32 * c);
+          }
+        }
         if (has_b && (x == 1 || u > 0)) {
           ok = mbar_wait_warp(&turn[x], (x == 1 ? u : u - 1) & 1, &abort_flag, p.status, 305 + x);
           if (!ok) break;
         }
-        if (x == 0 ? tiles.vis_a(j) : tiles.vis_b(j)) {
+        if (vis) {
           ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
           if (!ok) break;
           tc_fence_after();
           softmax_tile<kDrop>(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0,
-                              p.scale_log2, n == 0, m, l, &p_half[x], p.drop, (uint32_t)bh);
+                              p.scale_log2, n == 0, m, l, &p_half[x], kbits);
           tc_fence_before();
           mbar_arrive_warp(&p_full[x]);
           ++n;

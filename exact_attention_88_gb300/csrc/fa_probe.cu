@@ -184,21 +184,7 @@ cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStre
 namespace {
 
 // Dropout keep mask out[bh][i][j] through the row path of the forward and dQ
-// kernels: a thread per (bh, row i, group of eight keys g).
-__global__ void dropout_mask_rows_kernel(uint8_t* out, int N, DropParams d) {
-  const int bh = blockIdx.z, i = blockIdx.y;
-  const int g = blockIdx.x * blockDim.x + threadIdx.x;
-  if (8 * g >= N) return;
-  const uint4 m = keep_group(d, (uint32_t)bh, i, g);
-  const uint32_t w[4] = {m.x, m.y, m.z, m.w};
-  uint8_t* row = out + ((size_t)bh * N + i) * N;
-#pragma unroll
-  for (int e = 0; e < 8; ++e)
-    if (8 * g + e < N) row[8 * g + e] = (uint8_t)((w[e >> 1] >> (16 * (e & 1))) & 1u);
-}
-
-// The same through the row path of the dQ kernel: a thread per (bh, row i,
-// 32 keys).
+// kernels: a thread per (bh, row i, 32 keys).
 __global__ void dropout_mask_rowbits_kernel(uint8_t* out, int N, DropParams d) {
   const int bh = blockIdx.z, i = blockIdx.y;
   const int key0 = 32 * (blockIdx.x * blockDim.x + threadIdx.x);
@@ -225,9 +211,6 @@ __global__ void dropout_mask_keys_kernel(uint8_t* out, int N, DropParams d) {
 cudaError_t launch_dropout_mask(uint8_t* out, int BH, int N, const DropParams& d, int path,
                                 cudaStream_t s) {
   if (path == 0) {
-    const int groups = (N + 7) / 8;
-    dropout_mask_rows_kernel<<<dim3((groups + 127) / 128, N, BH), 128, 0, s>>>(out, N, d);
-  } else if (path == 2) {
     const int chunks = (N + 31) / 32;
     dropout_mask_rowbits_kernel<<<dim3((chunks + 127) / 128, N, BH), 128, 0, s>>>(out, N, d);
   } else {

@@ -279,10 +279,9 @@ fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int 
 
 /* Diagnostic: writes the dropout keep mask Z (uint8 [B*H, N, N], 1 = kept)
  * of `dropout` with the device code of the attention kernels: path 0 as the
- * forward kernel draws it (a query row per thread, AND masks of bf16 pairs),
- * path 2 as the dQ kernel does (a query row per thread, 32 keep bits), path 1
- * as the dK/dV kernel does (a key per thread, the bits of each call shared
- * among eight lanes).  `out` is device memory of B*H*N*N bytes; N <= 4096. */
+ * forward and dQ kernels draw it (a query row per thread, 32 keep bits at a
+ * time), path 1 as the dK/dV kernel does (a key per thread, the bits of each
+ * call shared among eight lanes).  `out` is device memory of B*H*N*N bytes; N <= 4096. */
 fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_dropout* dropout,
                                 int path, void* stream);
 

@@ -228,6 +228,6 @@ def test_dropout_mask_diagnostic_rejects(fa):
     assert fa.lib.fa_debug_dropout_mask(None, 1, 1, 64, dr, 0, None) == 1
     assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, None, 0, None) == 1
     assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 5000, dr, 0, None) == 2
-    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, dr, 3, None) == 1
+    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, dr, 2, None) == 1
     assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, ctypes.byref(fa.FaDropout(1.0, 1, 2)), 0,
                                         None) == 1

@@ -1,5 +1,5 @@
-"""GPU tests of fused dropout: the keep mask the kernels draw (through each of
-their three code paths) equals the oracle's bit for bit, and the forward and
+"""GPU tests of fused dropout: the keep mask the kernels draw (through both of
+their code paths: a query row per thread, a key per thread) equals the oracle's bit for bit, and the forward and
 backward with dropout match the fp64 oracle with the same mask within the
 bf16 tolerances."""
 import numpy as np
@@ -14,7 +14,7 @@ from _gpu_helpers import TOL, f64, max_abs, rel_fro, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("path", [0, 1])
 @pytest.mark.parametrize("B,H,N,p,seed,offset", [
     (1, 1, 1, 0.5, 0, 0),
     (2, 3, 300, 0.1, 12345, 7),
