@@ -45,6 +45,11 @@ Readings taken where the pages are silent:
   * the block-sparse tile mask is one T x T 0/1 array shared by every (b, h),
     T = ceil(N / block).
 
+An additive score bias (optional argument `bias`, any array broadcastable to
+[B, H, N, N]: the "+ mask" term of the score definition taken as a tensor) is
+added to the scaled scores before the masks: S_ij = scale q_i . k_j + bias_ij;
+bias entries of -inf hide a key like a mask.
+
 Dropout (optional argument `dropout=(p, seed, offset)` of the whole-tensor and
 sampled-row functions) follows `oracle/dropout.py`: O = (P o Z) V / (1 - p)
 with the mask Z of that module, and the chain rule through it.
@@ -103,10 +108,25 @@ def _kv_len_of(kv_len, b):
 # the definition, one (b, h) slice at a time
 # --------------------------------------------------------------------------
 
-def scores(q, k, scale, vis):
-    """S = scale * q k^T with -inf where a key is not visible.  q: [R,d], k: [N,d]."""
+def scores(q, k, scale, vis, bias=None):
+    """S = scale * q k^T (+ bias [R,N]) with -inf where a key is not visible.
+    q: [R,d], k: [N,d]."""
     s = scale * (np.asarray(q, np.float64) @ np.asarray(k, np.float64).T)
+    if bias is not None:
+        s = s + np.asarray(bias, np.float64)
     return np.where(vis, s, -np.inf)
+
+
+def _bias_of(bias, b, h):
+    """The [N, N] bias of slice (b, h) (broadcast over size-1 leading axes)."""
+    if bias is None:
+        return None
+    bias = np.asarray(bias)
+    return bias[b if bias.shape[0] > 1 else 0, h if bias.shape[1] > 1 else 0]
+
+
+def _rows(x, r):
+    return None if x is None else x[r]
 
 
 def probabilities(s):
@@ -136,18 +156,18 @@ def _drop(dropout, rows, cols, bh):
     return _dropout.keep_mask(rows, cols, bh, p, seed, offset), _dropout.keep_scale(p)
 
 
-def _slice_forward(q, k, v, scale, vis, z=None, rp=1.0):
-    p, lse = probabilities(scores(q, k, scale, vis))
+def _slice_forward(q, k, v, scale, vis, z=None, rp=1.0, bias=None):
+    p, lse = probabilities(scores(q, k, scale, vis, bias))
     pd = p if z is None else p * z * rp
     return pd @ np.asarray(v, np.float64), lse, p
 
 
-def _slice_backward(q, k, v, do, scale, vis, z=None, rp=1.0):
+def _slice_backward(q, k, v, do, scale, vis, z=None, rp=1.0, bias=None):
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     do = np.asarray(do, np.float64)
-    p, _ = probabilities(scores(q, k, scale, vis))
+    p, _ = probabilities(scores(q, k, scale, vis, bias))
     pd = p if z is None else p * z * rp
     dv = pd.T @ do
     dp = do @ v.T
@@ -165,7 +185,7 @@ def _slice_backward(q, k, v, do, scale, vis, z=None, rp=1.0):
 # --------------------------------------------------------------------------
 
 def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, block=128,
-            dropout=None):
+            dropout=None, bias=None):
     """O [B,H,N,d] and lse [B,H,N] (natural log) for q, k, v of shape [B,H,N,d]."""
     B, H, N, d = q.shape
     o = np.zeros((B, H, N, d), np.float64)
@@ -174,12 +194,13 @@ def forward(q, k, v, scale, causal=False, kv_len=None, block_mask=None, block=12
         vis = visible(N, k.shape[2], causal, _kv_len_of(kv_len, b), block_mask, block)
         for h in range(H):
             z, rp = _drop(dropout, np.arange(N), np.arange(k.shape[2]), b * H + h)
-            o[b, h], lse[b, h], _ = _slice_forward(q[b, h], k[b, h], v[b, h], scale, vis, z, rp)
+            o[b, h], lse[b, h], _ = _slice_forward(q[b, h], k[b, h], v[b, h], scale, vis, z, rp,
+                                                   _bias_of(bias, b, h))
     return o, lse
 
 
 def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, block=128,
-             dropout=None):
+             dropout=None, bias=None):
     """(dQ, dK, dV, D) for the loss sum(O * dO); D [B,H,N] = rowsum(P o dP)."""
     B, H, N, d = q.shape
     dq = np.zeros((B, H, N, d), np.float64)
@@ -191,7 +212,7 @@ def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, blo
         for h in range(H):
             z, rp = _drop(dropout, np.arange(N), np.arange(k.shape[2]), b * H + h)
             dq[b, h], dk[b, h], dv[b, h], dd[b, h] = _slice_backward(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, vis, z, rp)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, vis, z, rp, _bias_of(bias, b, h))
     return dq, dk, dv, dd
 
 
@@ -200,7 +221,7 @@ def backward(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None, blo
 # --------------------------------------------------------------------------
 
 def forward_rows(q, k, v, scale, rows, causal=False, kv_len=None, block_mask=None,
-                 block=128, dropout=None):
+                 block=128, dropout=None, bias=None):
     """O and lse of the selected query rows; rows: int array [B,H,R]."""
     B, H, N, d = q.shape
     R = rows.shape[2]
@@ -211,12 +232,13 @@ def forward_rows(q, k, v, scale, rows, causal=False, kv_len=None, block_mask=Non
             vis = visible(rows[b, h], N, causal, _kv_len_of(kv_len, b), block_mask, block)
             z, rp = _drop(dropout, rows[b, h], np.arange(N), b * H + h)
             o[b, h], lse[b, h], _ = _slice_forward(q[b, h][rows[b, h]], k[b, h],
-                                                   v[b, h], scale, vis, z, rp)
+                                                   v[b, h], scale, vis, z, rp,
+                                                   _rows(_bias_of(bias, b, h), rows[b, h]))
     return o, lse
 
 
 def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
-                        block_mask=None, block=128, dropout=None):
+                        block_mask=None, block=128, dropout=None, bias=None):
     """dQ of the selected query rows.  Everything dQ_i needs is in row i:
     P_i., dP_i. = dO_i V^T, D_i = sum_j P_ij dP_ij."""
     B, H, N, d = q.shape
@@ -226,7 +248,8 @@ def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
         for h in range(H):
             r = rows[b, h]
             vis = visible(r, N, causal, _kv_len_of(kv_len, b), block_mask, block)
-            p, _ = probabilities(scores(q[b, h][r], k[b, h], scale, vis))
+            p, _ = probabilities(scores(q[b, h][r], k[b, h], scale, vis,
+                                        _rows(_bias_of(bias, b, h), r)))
             dp = np.asarray(do[b, h][r], np.float64) @ np.asarray(v[b, h], np.float64).T
             z, rp = _drop(dropout, r, np.arange(N), b * H + h)
             if z is not None:
@@ -238,7 +261,7 @@ def backward_query_rows(q, k, v, do, scale, rows, causal=False, kv_len=None,
 
 
 def row_stats(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None,
-              block=128, rows_per_group=1024, dropout=None):
+              block=128, rows_per_group=1024, dropout=None, bias=None):
     """lse_i and D_i = sum_j P_ij dP_ij for EVERY query row, [B,H,N] each.
 
     Rows are taken a group at a time so that the score rows of a long
@@ -253,7 +276,8 @@ def row_stats(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None,
             for r0 in range(0, N, rows_per_group):
                 r = np.arange(r0, min(N, r0 + rows_per_group))
                 vis = visible(r, N, causal, _kv_len_of(kv_len, b), block_mask, block)
-                p, lse[b, h, r] = probabilities(scores(q[b, h][r], kf, scale, vis))
+                p, lse[b, h, r] = probabilities(scores(q[b, h][r], kf, scale, vis,
+                                                       _rows(_bias_of(bias, b, h), r)))
                 dp = np.asarray(do[b, h][r], np.float64) @ vf.T
                 z, rp = _drop(dropout, r, np.arange(N), b * H + h)
                 if z is not None:
@@ -263,7 +287,7 @@ def row_stats(q, k, v, do, scale, causal=False, kv_len=None, block_mask=None,
 
 
 def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=None,
-                      block_mask=None, block=128, dropout=None):
+                      block_mask=None, block=128, dropout=None, bias=None):
     """dK and dV of the selected key rows (cols: int array [B,H,C]).
 
     dK_j and dV_j sum over every query row, so they need every row's lse and
@@ -280,7 +304,8 @@ def backward_key_rows(q, k, v, do, scale, cols, lse, dd, causal=False, kv_len=No
             qf = np.asarray(q[b, h], np.float64)
             dof = np.asarray(do[b, h], np.float64)
             vis = visible(rows, N, causal, _kv_len_of(kv_len, b), block_mask, block, keys=c)
-            s = scores(qf, k[b, h][c], scale, vis)                  # [N, C]
+            bb = _bias_of(bias, b, h)
+            s = scores(qf, k[b, h][c], scale, vis, None if bb is None else bb[:, c])  # [N, C]
             l = lse[b, h][:, None]
             with np.errstate(invalid="ignore"):
                 p = np.where(vis & np.isfinite(l), np.exp(s - np.where(np.isfinite(l), l, 0.0)), 0.0)
