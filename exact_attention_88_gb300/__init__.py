@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "FaError", "FaMask", "FaLayout", "FaLayouts", "FaDropout", "FaOptions", "layout_of",
+    "FaError", "FaMask", "FaLayout", "FaLayouts", "FaDropout", "FaBias", "FaOptions", "layout_of",
+    "bias_of",
     "make_layouts", "make_options", "fa_fwd_ex", "fa_bwd_ex", "fa_fwd_fp32_ex", "fa_bwd_fp32_ex",
     "fa_bwd_preprocess_ex", "fa_bwd_dkdv_ex", "fa_bwd_dq_ex", "fa_debug_dropout_mask",
     "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
@@ -66,9 +67,16 @@ class FaDropout(ctypes.Structure):
     _fields_ = [("p", ctypes.c_float), ("seed", ctypes.c_uint64), ("offset", ctypes.c_uint32)]
 
 
+class FaBias(ctypes.Structure):
+    """Additive score bias (fa_bias): fp32 device pointer and element strides."""
+    _fields_ = [("ptr", ctypes.c_void_p), ("batch", ctypes.c_int64), ("head", ctypes.c_int64),
+                ("row", ctypes.c_int64)]
+
+
 class FaOptions(ctypes.Structure):
     """Options of the *_ex calls (fa_options)."""
-    _fields_ = [("layouts", ctypes.POINTER(FaLayouts)), ("dropout", ctypes.POINTER(FaDropout))]
+    _fields_ = [("layouts", ctypes.POINTER(FaLayouts)), ("dropout", ctypes.POINTER(FaDropout)),
+                ("bias", ctypes.POINTER(FaBias))]
 
 
 if not os.path.exists(LIB_PATH):
@@ -172,12 +180,26 @@ def make_layouts(**tensors):
     return ls
 
 
-def make_options(layouts=None, dropout_p=0.0, seed=0, offset=0):
+def bias_of(t):
+    """FaBias of a CUDA fp32 tensor broadcastable to [B, H, N, N] (4-D, last
+    dimension contiguous); dimensions of size 1 are broadcast (stride 0)."""
+    if t.dim() != 4:
+        raise ValueError("the bias must be 4-D: [B or 1, H or 1, N, N]")
+    if t.stride(3) != 1:
+        raise ValueError("the bias columns must be contiguous")
+    st = [0 if t.shape[i] == 1 else t.stride(i) for i in range(3)]
+    return FaBias(t.data_ptr(), st[0], st[1], st[2])
+
+
+def make_options(layouts=None, dropout_p=0.0, seed=0, offset=0, bias=None):
     """A pointer to an FaOptions: `layouts` an FaLayouts (or None: dense),
-    dropout with probability dropout_p (0: none), generator seed and offset.
-    The pointer keeps its members alive."""
+    dropout with probability dropout_p (0: none), generator seed and offset,
+    `bias` an FaBias (or None).  The pointer keeps its members alive."""
     opt = FaOptions()
     keep = []
+    if bias is not None:
+        keep.append(bias)
+        opt.bias = ctypes.pointer(bias)
     if layouts is not None:
         keep.append(layouts)
         opt.layouts = ctypes.pointer(layouts)
@@ -335,25 +357,28 @@ def _shape(q, *others):
 
 
 def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None,
-            dropout_p=0.0, seed=0, offset=0):
+            dropout_p=0.0, seed=0, offset=0, bias=None):
     """(O, lse) for CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32) of any layout
     whose last dimension is contiguous; O takes q's layout where torch can
     keep it (torch.empty_like).  dropout_p > 0 drops attention probabilities
-    (bf16 only); the backward needs the same dropout_p, seed and offset."""
+    (bf16 only); the backward needs the same dropout_p, seed and offset.
+    bias: fp32 tensor broadcastable to [B, H, N, N] added to the scaled
+    scores (bf16 only); the backward needs it too."""
     import torch
     B, H, N, d = _shape(q, k, v)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     mask = make_mask(kv_len, block_mask)
-    opt = make_options(make_layouts(q=q, k=k, v=v, o=o), dropout_p, seed, offset)
+    opt = make_options(make_layouts(q=q, k=k, v=v, o=o), dropout_p, seed, offset,
+                       None if bias is None else bias_of(bias))
     fn = fa_fwd_ex if q.dtype == torch.bfloat16 else fa_fwd_fp32_ex
     fn(q, k, v, o, lse, B, H, N, d, scale, causal, mask, opt, stream)
     return o, lse
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_mask=None,
-             stream=None, workspace=None, dropout_p=0.0, seed=0, offset=0):
+             stream=None, workspace=None, dropout_p=0.0, seed=0, offset=0, bias=None):
     """(dQ, dK, dV) for the forward above and output gradient do; each
     gradient takes the layout of its input where torch can keep it."""
     import torch
@@ -365,7 +390,7 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_m
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
     mask = make_mask(kv_len, block_mask)
     layouts = make_layouts(q=q, k=k, v=v, o=o, dO=do, dq=dq, dk=dk, dv=dv)
-    opt = make_options(layouts, dropout_p, seed, offset)
+    opt = make_options(layouts, dropout_p, seed, offset, None if bias is None else bias_of(bias))
     fn = fa_bwd_ex if q.dtype == torch.bfloat16 else fa_bwd_fp32_ex
     fn(q, k, v, o, do, lse, dq, dk, dv, workspace, ws_bytes, B, H, N, d, scale, causal, mask,
        opt, stream)

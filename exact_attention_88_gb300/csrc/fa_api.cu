@@ -101,6 +101,27 @@ fa_status check_layout(const fa_layout* in, int B, int H, int N, int d, int esiz
   return FA_OK;
 }
 
+// Validates an additive bias: pointer 16-byte aligned, strides >= 0 and
+// multiples of 4 elements (16 bytes: rows are read 4 floats at a time), the
+// row stride 0 or >= N.
+fa_status check_bias(const fa_bias* bias, int N, int esize, const float** ptr, Layout* lb) {
+  *ptr = nullptr;
+  *lb = Layout{0, 0, 0};
+  if (!bias) return FA_OK;
+  if (esize != 2) return FA_ERR_UNSUPPORTED;
+  if (!bias->ptr) return FA_ERR_INVALID_ARG;
+  if (!aligned16(bias->ptr)) return FA_ERR_ALIGNMENT;
+  const long long st[3] = {(long long)bias->batch, (long long)bias->head, (long long)bias->row};
+  for (long long x : st) {
+    if (x < 0 || x >= (1ll << 40)) return FA_ERR_UNSUPPORTED;
+    if (x % 4 != 0) return FA_ERR_ALIGNMENT;
+  }
+  if (st[2] != 0 && st[2] < N) return FA_ERR_UNSUPPORTED;
+  *ptr = bias->ptr;
+  *lb = Layout{st[0], st[1], st[2]};
+  return FA_OK;
+}
+
 // Validates a dropout request and derives the kernels' parameters: the
 // 16-bit threshold t = min(65535, floor(p 65536 + 1/2)) (keep probability
 // 1 - t/65536 exactly) and the scale 65536 / (65536 - t).  No request, or
@@ -171,6 +192,7 @@ static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* 
   if (st != FA_OK) return st;
   const fa_layouts* L = opt ? opt->layouts : nullptr;
   if ((st = check_dropout(opt ? opt->dropout : nullptr, esize, &a->drop)) != FA_OK) return st;
+  if ((st = check_bias(opt ? opt->bias : nullptr, N, esize, &a->bias, &a->lb)) != FA_OK) return st;
   if ((st = check_layout(L ? &L->q : nullptr, B, H, N, d, esize, &a->lq)) != FA_OK ||
       (st = check_layout(L ? &L->k : nullptr, B, H, N, d, esize, &a->lk)) != FA_OK ||
       (st = check_layout(L ? &L->v : nullptr, B, H, N, d, esize, &a->lv)) != FA_OK ||
@@ -197,6 +219,7 @@ static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float s
   if (st != FA_OK) return st;
   const fa_layouts* L = opt ? opt->layouts : nullptr;
   if ((st = check_dropout(opt ? opt->dropout : nullptr, esize, &a->drop)) != FA_OK) return st;
+  if ((st = check_bias(opt ? opt->bias : nullptr, N, esize, &a->bias, &a->lb)) != FA_OK) return st;
   const fa_layout* in[8] = {L ? &L->q : nullptr,  L ? &L->k : nullptr,  L ? &L->v : nullptr,
                             L ? &L->o : nullptr,  L ? &L->dO : nullptr, L ? &L->dq : nullptr,
                             L ? &L->dk : nullptr, L ? &L->dv : nullptr};

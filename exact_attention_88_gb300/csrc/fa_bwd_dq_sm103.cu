@@ -56,6 +56,8 @@ struct DqParams {
   __nv_bfloat16* dq;
   Layout ldq;
   DropParams drop;
+  const float* bias;  // additive score bias or nullptr
+  Layout lb;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -73,7 +75,7 @@ struct KTileIter {
   __device__ int next(int j) const { return bits ? next_tile_bit(bits, j, jend) : j; }
 };
 
-template <int D, bool kDrop>
+template <int D, bool kExtra>
 __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -276,6 +278,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       nd = -p.Dvec[(size_t)bh * p.N + q];
     }
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nl22 = make_float2(nl2, nl2);
+    // additive bias: this query row's bias (nullptr past the end of the sequence)
+    const bool bias_on = kExtra && p.bias != nullptr;
+    const float* brow = (bias_on && q < p.N) ? p.bias + row_offset(p.lb, b, hd, q) : nullptr;
     const float2 sc2 = make_float2(p.scale, p.scale), nd2 = make_float2(nd, nd);
     int u = 0;
     bool ok = true;
@@ -286,15 +291,18 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
       // causal, key <= q
       const int key0 = j * 128 + col0;
-      // dropout: keep bits of the 32 keys, drawn while S is computed
-      const uint32_t keep = kDrop ? keep_bits_of_row(p.drop, (uint32_t)bh, q, key0) : 0u;
+      // dropout: keep bits of the 32 keys (all set without dropout); bias:
+      // the 32 keys' bias, times log2(e), in pf -- both read while S is computed
+      const uint32_t keep =
+          kExtra ? (p.drop.t ? keep_bits_of_row(p.drop, (uint32_t)bh, q, key0) : ~0u) : 0u;
+      float pf[32];
+      if (kExtra && bias_on) load_bias_row<32>(brow, key0, p.N, pf);
       ok = mbar_wait_warp(&s_full, u & 1, &abort_flag, p.status, 901);
       if (!ok) break;
       tc_fence_after();
       int lim = kv_limit - key0;
       if (p.causal) lim = min(lim, q - key0 + 1);
       const bool partial = lim < 32;
-      float pf[32];
       uint32_t rs_all[32];
       FA_TMEM_LD32_SYNC(tS, rs_all);
 #pragma unroll
@@ -302,7 +310,8 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         const uint32_t* rs = rs_all + 16 * h;
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          const float2 t = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl22);
+          float2 t = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2, nl22);
+          if (kExtra && bias_on) t = add2(t, make_float2(pf[16 * h + e], pf[16 * h + e + 1]));
           pf[16 * h + e] = ex2(t.x);
           pf[16 * h + e + 1] = ex2(t.y);
         }
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
         for (int e = 0; e < 16; e += 2) {
           const float2 dpv = make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1]));
           float2 t;
-          if constexpr (kDrop) {
+          if constexpr (kExtra) {
             // dS = P o (Z o dP / (1 - p) - D): dropped entries keep only -D
             const int c = 16 * h + e;
             const float2 zr = make_float2(((keep >> c) & 1u) ? p.drop.rp : 0.f,
@@ -417,7 +426,9 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
   p.causal = a.causal;
   p.status = a.status;
   p.drop = a.drop;
-  auto kernel = a.drop.t ? fa_bwd_dq_kernel<D, true> : fa_bwd_dq_kernel<D, false>;
+  p.bias = a.bias;
+  p.lb = a.lb;
+  auto kernel = (a.drop.t || a.bias) ? fa_bwd_dq_kernel<D, true> : fa_bwd_dq_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

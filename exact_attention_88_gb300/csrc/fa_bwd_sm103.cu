@@ -64,6 +64,8 @@ struct BwdParams {
   __nv_bfloat16* dv;
   Layout ldk, ldv;
   DropParams drop;
+  const float* bias;  // additive score bias or nullptr
+  Layout lb;
   const int32_t* kv_len;
   const uint8_t* block_mask;
   int H, N, T, BH;
@@ -96,7 +98,7 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   }
 }
 
-template <int D, bool kDrop>
+template <int D, bool kExtra>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -307,6 +309,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int col0 = wg * 32;               // this warpgroup's query columns
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2);
     const float2 sc2 = make_float2(p.scale, p.scale);
+    const bool bias_on = kExtra && p.bias != nullptr;
     int it = 0;
     bool ok = true;
     // Statistics of one query row: loaded raw (lse, D) by a thread of the
@@ -342,10 +345,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // thread is past this tile's dS (the loads' latency hides behind the MMAs)
       RowStats next_st{};
       if (tid < 128) next_st = load_stats(qtiles.next(i + 1));
-      // dropout: keep bits of this key for the warpgroup's 32 query rows,
-      // drawn while S^T is computed
+      // dropout: keep bits of this key for the warpgroup's 32 query rows (all
+      // set without dropout); bias: bias[query][key] times log2(e) of those rows,
+      // in pf -- both read while S^T is computed
       const uint32_t keep =
-          kDrop ? keep_bits_of_key(p.drop, (uint32_t)bh, key, i * 128 + col0) : 0u;
+          kExtra ? (p.drop.t ? keep_bits_of_key(p.drop, (uint32_t)bh, key, i * 128 + col0) : ~0u)
+                 : 0u;
+      float pf[32];
+      if (kExtra && bias_on) {
+        const int qr0 = i * 128 + col0;
+        const float* bcol = p.bias + row_offset(p.lb, b, hd, qr0) + key;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          pf[c] = (key < p.N && qr0 + c < p.N) ? __ldg(bcol + (long long)c * p.lb.n) * kLog2e : 0.f;
+      }
       ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
       if (ok) ok = mbar_wait_warp(&s_ready, it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
@@ -355,7 +368,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // ---- P^T for the warpgroup's 32 columns (while dP^T is computed); packed
       // P^T of half h goes over S^T columns [col0 + 8h, col0 + 8h + 8), which
       // were read in half 0
-      float pf[32];
       uint32_t rs_all[32];
       FA_TMEM_LD32_SYNC(tmem + C::kColS + lane_off + col0, rs_all);
 #pragma unroll
@@ -368,8 +380,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 4 * g + 2 * u;
-            const float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])),
-                                  c2, u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
+            float2 x = fma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2,
+                            u ? make_float2(L.z, L.w) : make_float2(L.x, L.y));
+            if (kExtra && bias_on) x = add2(x, make_float2(pf[16 * h + e], pf[16 * h + e + 1]));
             pf[16 * h + e] = ex2(x.x);
             pf[16 * h + e + 1] = ex2(x.y);
           }
@@ -383,7 +396,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           float a0 = pf[16 * h + e], a1 = pf[16 * h + e + 1];
-          if constexpr (kDrop) {  // dV takes (P o Z)^T; the 1 / (1 - p) is applied at the end
+          if constexpr (kExtra) {  // dV takes (P o Z)^T; the 1 / (1 - p) is applied at the end
             if (!((keep >> (16 * h + e)) & 1u)) a0 = 0.f;
             if (!((keep >> (16 * h + e + 1)) & 1u)) a1 = 0.f;
           }
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             const float2 dpv = make_float2(__uint_as_float(rp[e]), __uint_as_float(rp[e + 1]));
             const float2 nD = u ? make_float2(Dd.z, Dd.w) : make_float2(Dd.x, Dd.y);
             float2 t;
-            if constexpr (kDrop) {
+            if constexpr (kExtra) {
               // dS^T = P^T o (Z o dP^T / (1 - p) - D): dropped entries keep only -D
               const int c = 16 * h + e;
               const float2 zr = make_float2(((keep >> c) & 1u) ? p.drop.rp : 0.f,
@@ -470,7 +483,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         if (key < p.N)
           store_row_bf16(which == 0 ? p.dv + base_v : p.dk + base_k, rr, C::kDSlice,
-                         (kDrop && which == 0) ? p.drop.rp : 1.f);
+                         (kExtra && which == 0) ? p.drop.rp : 1.f);
       }
     }
   }
@@ -502,6 +515,8 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   p.ldk = a.ldk;
   p.ldv = a.ldv;
   p.drop = a.drop;
+  p.bias = a.bias;
+  p.lb = a.lb;
   p.kv_len = a.mask_kind == FA_MASK_KEY_PADDING ? a.kv_len : nullptr;
   p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
   p.H = a.H;
@@ -512,7 +527,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
-  auto kernel = a.drop.t ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;
+  auto kernel = (a.drop.t || a.bias) ? fa_bwd_dkdv_kernel<D, true> : fa_bwd_dkdv_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

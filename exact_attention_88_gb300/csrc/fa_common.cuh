@@ -249,6 +249,31 @@ __device__ __forceinline__ uint32_t keep_bits_of_key(const DropParams& d, uint32
   return out;
 }
 
+// ---------------------------------------------------------------------------
+// Additive score bias: kCount values of keys [k0, k0 + kCount) of one bias
+// row, times log2(e) (the kernels work in base 2); 0 past n_keys or without a
+// row (brow nullptr: a query row past the end).  The row is 16-byte aligned
+// and k0 a multiple of 4, so whole rows are read 4 floats at a time.
+// ---------------------------------------------------------------------------
+template <int kCount>
+__device__ __forceinline__ void load_bias_row(const float* brow, int k0, int n_keys, float* out) {
+  constexpr float kL2e = 1.4426950408889634f;
+  if (brow && k0 + kCount <= n_keys) {
+#pragma unroll
+    for (int g = 0; g < kCount / 4; ++g) {
+      const float4 t = __ldg(reinterpret_cast<const float4*>(brow + k0) + g);
+      out[4 * g] = t.x * kL2e;
+      out[4 * g + 1] = t.y * kL2e;
+      out[4 * g + 2] = t.z * kL2e;
+      out[4 * g + 3] = t.w * kL2e;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kCount; ++e)
+      out[e] = (brow && k0 + e < n_keys) ? __ldg(brow + k0 + e) * kL2e : 0.f;
+  }
+}
+
 // One arrival for the whole warp, made by lane 0 once every lane has got
 // here: the lanes' earlier writes (completed TMEM stores, shared-memory
 // stores fenced for the async proxy) are ordered before it by the warp sync.

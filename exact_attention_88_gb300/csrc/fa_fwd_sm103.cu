@@ -53,6 +53,8 @@ struct FwdParams {
   __nv_bfloat16* o;
   Layout lo;
   DropParams drop;
+  const float* bias;  // additive score bias or nullptr
+  Layout lb;
   float* lse;
   const int32_t* kv_len;
   const uint8_t* block_mask;
@@ -106,17 +108,42 @@ __device__ __forceinline__ float max64(const uint32_t* r) {
   return fmaxf(max3(mx[0], mx[1], mx[2]), max3(mx[3], max3(mx[4], mx[5], mx[6]), mx[7]));
 }
 
-template <bool kDrop>
+// kExtra: the variant with dropout (kbits) and an additive bias (brow: this
+// row's bias, nullptr past the end; bias_on warp-uniform).
+template <bool kExtra>
 __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols32, int key0,
                                              int kv_limit, int row, bool causal, float scale_log2,
                                              bool first, float& m, float& l, uint64_t* p_half,
-                                             const uint32_t* kbits) {
+                                             const uint32_t* kbits, bool bias_on,
+                                             const float* brow, int n_keys) {
   // keys [0, lim) of the tile are visible from this row
   int lim = kv_limit - key0;
   if (causal) lim = min(lim, row - key0 + 1);
   const bool partial = lim < 128;
   float tmax;
-  {
+  float exp_scale = scale_log2;  // multiplies what the exponent pass reads from tS
+  if (kExtra && bias_on) {
+    // biased scores in log2 units, S scale log2(e)... + bias log2(e), written back
+    // over S so that the exponent pass reads them directly
+    tmax = -INFINITY;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      uint32_t r[64];
+      float bv[64];
+      FA_TMEM_LD64_SYNC(tS + 64 * half, r);
+      if (partial) mask_tail(r, lim - 64 * half);
+      load_bias_row<64>(brow, key0 + 64 * half, n_keys, bv);
+#pragma unroll
+      for (int e = 0; e < 64; ++e)
+        r[e] = __float_as_uint(fmaf(__uint_as_float(r[e]), scale_log2, bv[e]));
+      tmax = fmaxf(tmax, max64(r));
+      const uint32_t* r_hi = r + 32;
+      FA_TMEM_ST32(tS + 64 * half, r);
+      FA_TMEM_ST32(tS + 64 * half + 32, r_hi);
+    }
+    tmem_wait_st();
+    exp_scale = 1.f;
+  } else {
     uint32_t r[64];
     FA_TMEM_LD64_SYNC(tS, r);
     if (partial) mask_tail(r, lim);
@@ -124,8 +151,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     FA_TMEM_LD64_SYNC(tS + 64, r);
     if (partial) mask_tail(r, lim - 64);
     tmax = fmaxf(tmax, max64(r));
+    tmax *= scale_log2;
   }
-  const float m_tile = tmax * scale_log2;
+  const float m_tile = tmax;
   const float m_new = fmaxf(m, m_tile);
   const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
   float alpha = 1.f;
@@ -146,7 +174,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     }
   }
   const float nm = (m == -INFINITY) ? 0.f : -m;
-  const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
+  const float2 c2 = make_float2(exp_scale, exp_scale), nm2 = make_float2(nm, nm);
   float2 acc[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) acc[k] = make_float2(0.f, 0.f);
@@ -157,14 +185,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
     if (partial) mask_tail(r, lim - 64 * half);
     uint32_t pk[32];
     // dropout: keep bits of this half's keys [0, 32) and [32, 64)
-    const uint32_t kb0 = kDrop ? (half ? kbits[2] : kbits[0]) : 0u;
-    const uint32_t kb1 = kDrop ? (half ? kbits[3] : kbits[1]) : 0u;
+    const uint32_t kb0 = kExtra ? (half ? kbits[2] : kbits[0]) : 0u;
+    const uint32_t kb1 = kExtra ? (half ? kbits[3] : kbits[1]) : 0u;
 #pragma unroll
     for (int e = 0; e < 64; e += 2) {
       const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
       float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
       acc[(e >> 1) & 7] = add2(acc[(e >> 1) & 7], pv);  // l sums the undropped P~
-      if constexpr (kDrop) {
+      if constexpr (kExtra) {  // dropout (all bits set without it)
         const uint32_t kb = e < 32 ? kb0 : kb1;
         if (!((kb >> (e & 31)) & 1u)) pv.x = 0.f;
         if (!((kb >> ((e + 1) & 31)) & 1u)) pv.y = 0.f;
@@ -189,7 +217,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
   tmem_wait_st();
 }
 
-template <int D, bool kDrop>
+template <int D, bool kExtra>
 __global__ void __launch_bounds__(352, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -378,6 +406,9 @@ __global__ void __launch_bounds__(352, 1)
     int n = 0;
     bool ok = true;
     const bool live_tile = x == 0 || has_b;
+    // additive bias: this row's [N] bias (nullptr past the end of the sequence)
+    const bool bias_on = kExtra && p.bias != nullptr;
+    const float* brow = (bias_on && row < p.N) ? p.bias + row_offset(p.lb, b, hd, row) : nullptr;
     if (live_tile) {
       int u = 0;  // key tiles either tile sees, in order
       for (int j = tiles.next(0); j < tiles.end(); j = tiles.next(j + 1), ++u) {
@@ -388,9 +419,9 @@ __global__ void __launch_bounds__(352, 1)
         const bool vis = x == 0 ? tiles.vis_a(j) : tiles.vis_b(j);
         // dropout: this row's keep bits of the tile, drawn before the turn and S
         // are waited for (while the other warpgroup's softmax runs)
-        uint32_t kbits[4] = {0u, 0u, 0u, 0u};
-        if constexpr (kDrop) {
-          if (vis) {
+        uint32_t kbits[4] = {~0u, ~0u, ~0u, ~0u};
+        if constexpr (kExtra) {
+          if (vis && p.drop.t) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               kbits[c] = keep_bits_of_row(p.drop, (uint32_t)bh, row, j * 128 + 32 * c);
@@ -404,8 +435,9 @@ __global__ void __launch_bounds__(352, 1)
           ok = mbar_wait_warp(&s_full[x], n & 1, &abort_flag, p.status, 301 + x);
           if (!ok) break;
           tc_fence_after();
-          softmax_tile<kDrop>(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0,
-                              p.scale_log2, n == 0, m, l, &p_half[x], kbits);
+          softmax_tile<kExtra>(tS, tO, D / 32, j * 128, kv_limit, row, p.causal != 0,
+                               p.scale_log2, n == 0, m, l, &p_half[x], kbits, bias_on, brow,
+                               p.N);
           tc_fence_before();
           mbar_arrive_warp(&p_full[x]);
           ++n;
@@ -423,7 +455,7 @@ __global__ void __launch_bounds__(352, 1)
       if (__all_sync(0xffffffffu, !abort_flag)) {  // warp-uniform: TMEM loads below
         const bool empty_row = !(l > 0.f);
         // dropout: the kept entries of P are scaled by 1 / (1 - p)
-        const float inv = empty_row ? 0.f : (kDrop ? p.drop.rp : 1.f) / l;
+        const float inv = empty_row ? 0.f : (kExtra ? p.drop.rp : 1.f) / l;
         const long long base = row_offset(p.lo, b, hd, row);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -487,7 +519,9 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.causal = a.causal;
   p.status = a.status;
   p.drop = a.drop;
-  auto kernel = a.drop.t ? fa_fwd_kernel<D, true> : fa_fwd_kernel<D, false>;
+  p.bias = a.bias;
+  p.lb = a.lb;
+  auto kernel = (a.drop.t || a.bias) ? fa_fwd_kernel<D, true> : fa_fwd_kernel<D, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.pairs * BH);

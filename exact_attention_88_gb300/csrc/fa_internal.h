@@ -56,6 +56,8 @@ struct FwdArgs {
   float* lse;  // dense fp32 [B,H,N]
   Layout lq, lk, lv, lo;
   DropParams drop;
+  const float* bias;  // additive score bias (nullptr: none), strides lb
+  Layout lb;
   int B, H, N, d;
   float scale;
   int causal;
@@ -78,6 +80,8 @@ struct BwdArgs {
   void* dv;
   Layout lq, lk, lv, lo, ldo, ldq, ldk, ldv;
   DropParams drop;
+  const float* bias;
+  Layout lb;
   int B, H, N, d;
   float scale;
   int causal;

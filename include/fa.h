@@ -180,11 +180,27 @@ typedef struct {
   uint32_t offset;  /* fourth counter word: a new value per step (e.g. the step number) */
 } fa_dropout;
 
+/* Additive score bias: the "+ mask" term of the scores as a tensor,
+ *     S_ij = scale q_i . k_j + bias[b, h, i, j]
+ * added before the causal / padding / block masks (summary page, "Problem
+ * and motivation"; the masks of the glossary page "Flash Attention",
+ * "Normalization and Masking").  fp32 in device memory; element (b, h, i, j)
+ * at ptr + b*batch + h*head + i*row + j.  A stride of 0 broadcasts (one
+ * [N, N] bias for every head: batch = head = 0).  -inf hides a key; +inf
+ * and NaN are not allowed.  Rules: ptr 16-byte aligned; strides >= 0,
+ * multiples of 4 elements, row >= N unless 0 (FA_ERR_ALIGNMENT /
+ * FA_ERR_UNSUPPORTED otherwise).  The bias receives no gradient. */
+typedef struct {
+  const float* ptr;
+  int64_t batch, head, row;
+} fa_bias;
+
 /* Options of the *_ex calls.  NULL options, or NULL members, mean dense
- * tensors and no dropout. */
+ * tensors, no dropout and no bias. */
 typedef struct {
   const fa_layouts* layouts;
   const fa_dropout* dropout;  /* bf16 calls only: FA_ERR_UNSUPPORTED for fp32 */
+  const fa_bias* bias;        /* bf16 calls only: FA_ERR_UNSUPPORTED for fp32 */
 } fa_options;
 
 /* fa_fwd / fa_bwd / fa_fwd_fp32 / fa_bwd_fp32 and the three backward steps
@@ -193,7 +209,8 @@ typedef struct {
  * other layouts give the same results on the same values (the kernels read
  * and write through the strides -- the TMA descriptors of the bf16 kernels
  * carry them -- and nothing is copied).  Errors: a p outside [0, 1)
- * (or NaN) is FA_ERR_INVALID_ARG; dropout on an fp32 call, FA_ERR_UNSUPPORTED. */
+ * (or NaN) is FA_ERR_INVALID_ARG; dropout or a bias on an fp32 call,
+ * FA_ERR_UNSUPPORTED. */
 fa_status fa_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                     int N, int d, float scale, int causal, const fa_mask* mask,
                     const fa_options* options, void* stream);
@@ -210,7 +227,7 @@ fa_status fa_bwd_fp32_ex(const float* q, const float* k, const float* v, const f
                          float scale, int causal, const fa_mask* mask, const fa_options* options,
                          void* stream);
 /* The backward steps with options (layouts of o, dO for the preprocess;
- * dropout for fa_bwd_dkdv_ex and fa_bwd_dq_ex). */
+ * dropout and bias for fa_bwd_dkdv_ex and fa_bwd_dq_ex). */
 fa_status fa_bwd_preprocess_ex(const void* o, const void* dO, float* D, int B, int H, int N, int d,
                                const fa_options* options, void* stream);
 fa_status fa_bwd_dkdv_ex(const void* q, const void* k, const void* v, const void* dO,

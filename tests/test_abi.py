@@ -231,3 +231,28 @@ def test_dropout_mask_diagnostic_rejects(fa):
     assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, dr, 2, None) == 1
     assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, ctypes.byref(fa.FaDropout(1.0, 1, 2)), 0,
                                         None) == 1
+
+
+def test_bias_rules(fa):
+    def call(fp32=False, bwd=False, N=128, **bkw):
+        b = dict(ptr=FAKE, batch=0, head=0, row=N)
+        b.update(bkw)
+        bias = fa.FaBias(b["ptr"], b["batch"], b["head"], b["row"])
+        opt = fa.make_options(None, 0.0, 0, 0, bias)
+        if not bwd:
+            fn = fa.lib.fa_fwd_fp32_ex if fp32 else fa.lib.fa_fwd_ex
+            return fn(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, N, 64, 0.125, 0, None, opt, None)
+        ws = fa.fa_bwd_workspace_size(1, 2, N, 64)
+        fn = fa.lib.fa_bwd_fp32_ex if fp32 else fa.lib.fa_bwd_ex
+        return fn(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws, 1, 2, N, 64, 0.125,
+                  0, None, opt, None)
+    for bwd in (False, True):
+        assert call(bwd=bwd) == 5                          # valid: reaches CUDA (none here)
+        assert call(bwd=bwd, head=128 * 128, row=128) == 5
+        assert call(bwd=bwd, ptr=None) == 1
+        assert call(bwd=bwd, ptr=FAKE + 4) == 3
+        assert call(bwd=bwd, row=130) == 3                  # not a multiple of 4 elements
+        assert call(bwd=bwd, row=64) == 2                   # rows overlap (row < N)
+        assert call(bwd=bwd, head=-128) == 2
+        assert call(bwd=bwd, row=0) == 5                    # one row for every query
+        assert call(fp32=True, bwd=bwd) == 2                # fp32 path: no bias
