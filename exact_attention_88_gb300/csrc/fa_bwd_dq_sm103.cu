@@ -22,6 +22,13 @@
 // key columns [32w, 32w+32) of S / dP and d columns [w d/4, (w+1) d/4) of the
 // dQ read-out; warp 16 is the TMA producer; warps 17, 18, 19 issue S, dP and
 // dQ (one thread each).
+//
+// Inputs are read through 4-D TMA descriptors with their own strides; dQ is
+// stored through its strides.  A block-sparse CTA copies its row of the tile
+// mask into a shared-memory bitmap first.  The kExtra variant adds dropout
+// (a row's 32 keep bits of a key tile drawn before S is waited for; dS takes
+// the dropped form of dP) and an additive bias (the row's 32 bias values read
+// before S is waited for, added to the scaled scores).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 

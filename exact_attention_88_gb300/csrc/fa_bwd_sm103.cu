@@ -28,6 +28,14 @@
 // query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4)
 // of dK, dV; warp 16 is the TMA producer; warps 17 and 18 issue the MMAs
 // (S^T, dP^T and dV, dK respectively).
+//
+// Inputs are read through 4-D TMA descriptors with their own strides; dK, dV
+// are stored through theirs.  A block-sparse CTA copies its column of the tile
+// mask into a shared-memory bitmap first.  The kExtra variant adds dropout
+// (the keep bits of a key for 32 query rows, each Philox call drawn once by one
+// of eight lanes and shared through shuffles; dV takes (P o Z)^T, dS^T the
+// dropped form of dP^T, dV is scaled by 1/(1-p) at the end) and an additive bias
+// (bias[query][key] added to the scaled scores before the exponential).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 

@@ -25,6 +25,15 @@
 //   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
 //   warps 9, 10     MMA issuers for tile A, B (one thread each).
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
+//
+// Every tensor is read through a 4-D TMA descriptor (column, row, head, batch)
+// carrying its own strides, and O is stored through its strides, so any layout
+// with contiguous rows costs nothing.  A block-sparse CTA copies its two rows
+// of the tile mask into shared-memory bitmaps first.  The kExtra variant adds
+// dropout (a row's 128 keep bits of a tile are drawn before its turn; dropped
+// entries of P~ are zeroed after l has summed them; O is scaled by 1/(1-p) at
+// the end) and an additive bias (added to the scaled scores in the max pass,
+// the biased scores written back over S).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
