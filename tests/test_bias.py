@@ -107,3 +107,39 @@ def test_causal_bias_equals_causal_mask(fa):
     assert max_abs(l0.cpu().numpy().astype(np.float64), l1.cpu().numpy().astype(np.float64)) <= 1e-4
     for a, b in zip(g0, g1):
         assert rel_fro(f64(b), f64(a)) <= 1e-2
+
+
+def test_everything_together(fa):
+    """[B,N,H,d] inputs and outputs, a padded-row dO, dropout, a per-head bias,
+    causal and key padding in one call, against the oracle on dense arrays."""
+    B, H, N, d = 2, 3, 333, 128
+    rng = np.random.default_rng(12)
+    kv = rng.integers(100, N + 1, B)
+    case = random_case(B, H, N, d, seed=13, kv_len=kv)
+    t = to_device(case, "bf16")
+    bnhd = lambda x: x.transpose(1, 2).contiguous().transpose(1, 2)   # [B,N,H,d] storage
+    q, k, v = bnhd(t["q"]), bnhd(t["k"]), bnhd(t["v"])
+    do_buf = torch.zeros(B, H, N, d + 64, dtype=torch.bfloat16, device="cuda")
+    do_buf[..., :d] = t["do"]
+    do = do_buf[..., :d]
+    N4 = (N + 3) // 4 * 4
+    bias_np = rng.standard_normal((1, H, N, N)).astype(np.float32)
+    bias_buf = torch.zeros(1, H, N, N4, dtype=torch.float32, device="cuda")
+    bias_buf[..., :N] = torch.from_numpy(bias_np).cuda()
+    bias = bias_buf[..., :N]
+    drop = (0.15, 4242, 17)
+    kw = dict(kv_len=t["kv_len"], bias=bias, dropout_p=drop[0], seed=drop[1], offset=drop[2])
+    scale = d ** -0.5
+    o, lse = fa.forward(q, k, v, scale, True, **kw)
+    assert o.stride() == q.stride()
+    dq, dk, dv = fa.backward(q, k, v, o, do, lse, scale, True, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == 0
+    okw = dict(causal=True, kv_len=case["kv_len"], bias=bias_np.astype(np.float64), dropout=drop)
+    ro, rl = oracle.forward(case["q"], case["k"], case["v"], scale, **okw)
+    rdq, rdk, rdv, _ = oracle.backward(case["q"], case["k"], case["v"], case["do"], scale, **okw)
+    to, tl, tg = TOL["bf16"]
+    assert max_abs(f64(o), ro) <= to * D.keep_scale(drop[0])
+    assert max_abs(lse.cpu().numpy().astype(np.float64), rl, finite_only=True) <= tl
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), (rdq, rdk, rdv)):
+        assert rel_fro(f64(g), r) <= tg, name
