@@ -291,6 +291,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
     const float2 sc2 = make_float2(p.scale, p.scale), nd2 = make_float2(nd, nd);
     int u = 0;
     bool ok = true;
+    uint32_t keep_next = ~0u;  // dropout: the first key tile's keep bits
+    if (kExtra && p.drop.t && jfirst < ktiles.jend)
+      keep_next = keep_bits_of_row(p.drop, (uint32_t)bh, q, jfirst * 128 + col0);
     for (int j = jfirst; j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
       const int x = u & 1;  // dP buffer
       const uint32_t tS = tmem + C::kColS + lane_off + col0;
@@ -298,10 +301,10 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
       // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
       // causal, key <= q
       const int key0 = j * 128 + col0;
-      // dropout: keep bits of the 32 keys (all set without dropout); bias:
-      // the 32 keys' bias, times log2(e), in pf -- both read while S is computed
-      const uint32_t keep =
-          kExtra ? (p.drop.t ? keep_bits_of_row(p.drop, (uint32_t)bh, q, key0) : ~0u) : 0u;
+      // dropout: keep bits of the 32 keys (all set without dropout), drawn
+      // during the previous key tile; bias: the 32 keys' bias, times log2(e), in
+      // pf, read while S is computed
+      const uint32_t keep = kExtra ? keep_next : 0u;
       float pf[32];
       if (kExtra && bias_on) load_bias_row<32>(brow, key0, p.N, pf);
       ok = mbar_wait_warp(&s_full, u & 1, &abort_flag, p.status, 901);
@@ -330,6 +333,12 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e)
           if (e >= lim) pf[e] = 0.f;
+      }
+      // dropout: the next key tile's keep bits, drawn while dP is computed
+      if (kExtra && p.drop.t) {
+        const int jn = ktiles.next(j + 1);
+        keep_next = jn < ktiles.jend ? keep_bits_of_row(p.drop, (uint32_t)bh, q, jn * 128 + col0)
+                                     : ~0u;
       }
       ok = mbar_wait_warp(&dp_full[x], (u >> 1) & 1, &abort_flag, p.status, 902);
       if (!ok) break;

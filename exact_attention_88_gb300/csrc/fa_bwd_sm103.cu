@@ -342,6 +342,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       st.nd = -st.nd;
       return st;
     };
+    // dropout: the first tile's keep bits (every math lane takes part: shuffles)
+    uint32_t keep_next = ~0u;
+    if (kExtra && p.drop.t && iend > 0)
+      keep_next = keep_bits_of_key(p.drop, (uint32_t)bh, key, qtiles.first() * 128 + col0);
     if (tid < 128 && iend > 0) {
       const RowStats st = finish_stats(load_stats(qtiles.first()));
       s_nl2[tid] = st.nl2;
@@ -354,11 +358,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       RowStats next_st{};
       if (tid < 128) next_st = load_stats(qtiles.next(i + 1));
       // dropout: keep bits of this key for the warpgroup's 32 query rows (all
-      // set without dropout); bias: bias[query][key] times log2(e) of those rows,
-      // in pf -- both read while S^T is computed
-      const uint32_t keep =
-          kExtra ? (p.drop.t ? keep_bits_of_key(p.drop, (uint32_t)bh, key, i * 128 + col0) : ~0u)
-                 : 0u;
+      // set without dropout), drawn during the previous tile; bias:
+      // bias[query][key] times log2(e) of those rows, in pf, read while S^T is
+      // computed
+      const uint32_t keep = kExtra ? keep_next : 0u;
       float pf[32];
       if (kExtra && bias_on) {
         const int qr0 = i * 128 + col0;
@@ -415,6 +418,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&p_ready);
+      // dropout: the next tile's keep bits, drawn while dP^T is computed
+      if (kExtra && p.drop.t) {
+        const int inext = qtiles.next(i + 1);
+        keep_next = inext < iend
+                        ? keep_bits_of_key(p.drop, (uint32_t)bh, key, inext * 128 + col0)
+                        : ~0u;
+      }
       // ---- dS^T = scale P^T o (dP^T - D) (while dV is computed): packed bf16
       // over dP^T columns [col0, col0 + 16), which this thread has read
       ok = mbar_wait_warp(&dp_ready, it & 1, &abort_flag, p.status, 608);
