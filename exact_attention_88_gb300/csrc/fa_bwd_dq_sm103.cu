@@ -107,9 +107,9 @@ __global__ void __launch_bounds__(DqCfg<D>::kThreads, 1)
   __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask row qi
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lin = blockIdx.x;
-  const int qi = p.T - 1 - lin / p.BH;  // causal: the last query tiles see the most keys: first
-  const int bh = lin % p.BH;
+  int order, bh;
+  grid_order(blockIdx.x, p.BH, p.T, &order, &bh);
+  const int qi = p.T - 1 - order;  // causal: the last query tiles see the most keys: first
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   int kv_limit = p.N;

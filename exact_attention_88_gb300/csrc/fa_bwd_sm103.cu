@@ -130,9 +130,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask column kt
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int lin = blockIdx.x;
-  const int kt = lin / p.BH;  // key tile (causal: low tiles have the most work: first)
-  const int bh = lin % p.BH;
+  int kt, bh;  // key tile (causal: low tiles have the most work: first)
+  grid_order(blockIdx.x, p.BH, p.T, &kt, &bh);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   int kv_limit = p.N;

@@ -274,6 +274,24 @@ __device__ __forceinline__ void load_bias_row(const float* brow, int k0, int n_k
   }
 }
 
+// ---------------------------------------------------------------------------
+// Grid order: CTA lin -> (work-order index t, head bh) with the heads taken
+// kGroupHeads at a time, so that the CTAs resident at once share the K / V
+// (or Q / dO) tiles of a few heads in L2 instead of all of them; within a group
+// the order index runs slowest (t = 0 first: the callers put the heaviest
+// tiles there).  A last, smaller group takes the remaining heads.
+// ---------------------------------------------------------------------------
+constexpr int kGroupHeads = 8;
+
+__device__ __forceinline__ void grid_order(int lin, int BH, int nt, int* t, int* bh) {
+  const int per_group = kGroupHeads * nt;
+  const int g = lin / per_group;
+  const int r = lin - g * per_group;
+  const int gh = min(kGroupHeads, BH - g * kGroupHeads);  // heads in this group
+  *t = r / gh;
+  *bh = g * kGroupHeads + (r - *t * gh);
+}
+
 // One arrival for the whole warp, made by lane 0 once every lane has got
 // here: the lanes' earlier writes (completed TMEM stores, shared-memory
 // stores fenced for the async proxy) are ordered before it by the warp sync.

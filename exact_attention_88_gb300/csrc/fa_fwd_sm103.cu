@@ -247,9 +247,9 @@ __global__ void __launch_bounds__(352, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest pairs first (causal rows near the end see the most keys)
-  const int lin = blockIdx.x;
-  const int pair = p.pairs - 1 - lin / p.BH;
-  const int bh = lin % p.BH;
+  int order, bh;
+  grid_order(blockIdx.x, p.BH, p.pairs, &order, &bh);
+  const int pair = p.pairs - 1 - order;
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   const int qa = 2 * pair, qb = 2 * pair + 1;  // query tiles; qb may be past the end
