@@ -24,10 +24,10 @@
 //   dK += dS^T Q_i A from TMEM
 // so the next tile's S^T queues behind dK without waiting for it.
 //
-// Roles (608 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
+// Roles (640 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4)
-// of dK, dV; warp 16 is the TMA producer; warps 17 and 18 issue the MMAs
-// (S^T, dP^T and dV, dK respectively).
+// of dK, dV; warp 16 is the TMA producer; warps 17, 18 and 19 issue the MMAs
+// (S^T; dV, dK; dP^T).
 //
 // Inputs are read through 4-D TMA descriptors with their own strides; dK, dV
 // are stored through theirs.  A block-sparse CTA copies its column of the tile
@@ -61,7 +61,7 @@ struct BwdCfg {
   static constexpr uint32_t kColDV = 0, kColDK = D, kColS = 2 * D, kColDP = 2 * D + 128;
   static constexpr int kMathWarps = 16;
   static constexpr int kMathThreads = kMathWarps * 32;
-  static constexpr int kThreads = kMathThreads + 96;  // + producer, two MMA issuers
+  static constexpr int kThreads = kMathThreads + 128;  // + producer, three MMA issuers
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the dK / dV read-out
 };
 
@@ -115,12 +115,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, stats_ready, drain, drain_a;
-  // q_empty[s] completes when dK of the tile in Q stage s is done: it both frees
-  // the stage and tells the issuer that dS^T (in the dP^T columns) was read;
-  // do_empty[s] likewise for dV, the dO stage and P^T (in the S^T columns).
-  // One commit per tile each; per-stage barriers keep every waiter within
-  // one phase.
+  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, stats_ready, drain, drain_a,
+      drain_c;
+  // q_empty[s] completes when dK of the tile in Q stage s is done (dK is the
+  // last reader of Q_i: S^T was read before the math could produce dS^T): it
+  // both frees the stage and tells issuer C that dS^T (in the dP^T columns) was
+  // read.  do_empty[s] completes when both readers of dO_i, dV and dP^T, are
+  // done: it frees the dO stage and tells issuer A that P^T (in the S^T
+  // columns) was read.  Per-stage barriers keep every waiter within one phase.
   __shared__ uint64_t q_full[C::kQStages], q_empty[C::kQStages];
   __shared__ uint64_t do_full[C::kDOStages], do_empty[C::kDOStages];
   __shared__ __align__(16) float s_nl2[128];  // -lse2 of the tile's query rows
@@ -150,13 +152,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&stats_ready, 4);
     mbar_init(&drain, 1);
     mbar_init(&drain_a, 1);
+    mbar_init(&drain_c, 1);
     for (int s = 0; s < C::kQStages; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);  // dK, the last reader of Q_i, is done
     }
     for (int s = 0; s < C::kDOStages; ++s) {
       mbar_init(&do_full[s], 1);
-      mbar_init(&do_empty[s], 1);
+      mbar_init(&do_empty[s], 2);  // dO_i has two readers: dV (issuer B) and dP^T (issuer C)
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -217,15 +220,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int s = 0; s < C::kDOStages; ++s)
         if (dcount[s]) mbar_drain(&do_full[s], (dcount[s] - 1) & 1);
     }
-  } else if (warp == C::kMathWarps + 1 || warp == C::kMathWarps + 2) {
+  } else if (warp > C::kMathWarps) {
     // ------------------------------------------------------------ MMA issuers
-    // Two issuing threads, one per dependency chain, so that a wait on one
-    // chain never holds back the other's MMAs (an MMA costs its issuing thread
-    // about as long as the tensor core takes to run it):
-    //   A (warp 17): S^T and dP^T -- gated by the loads and by the previous
-    //                tile's dV / dK (the readers of the columns they overwrite)
-    //   B (warp 18): dV and dK    -- gated by the math (P^T, dS^T)
-    const bool issuer_a = warp == C::kMathWarps + 1;
+    // Three issuing threads, so that a wait on one dependency chain never holds
+    // back another's MMAs (an MMA costs its issuing thread about as long as the
+    // tensor core takes to run it):
+    //   A (warp 17): S^T  -- gated by Q_i and by the previous tile's dV (the
+    //                reader of the S^T columns, where P^T sits)
+    //   B (warp 18): dV and dK -- gated by the math (P^T, dS^T)
+    //   C (warp 19): dP^T -- gated by dO_i and by the previous tile's dK (the
+    //                reader of the dP^T columns, where dS^T sits)
+    const int role = warp - C::kMathWarps - 1;  // 0: A, 1: B, 2: C
+    const bool issuer_a = role == 0, issuer_c = role == 2;
     if (lane == 0 && iend > 0) {
       constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
@@ -235,15 +241,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // its byte offset >> 4 to the start-address field (every buffer lies
       // below 256 KB, so the 14-bit field never carries)
       const uint64_t dK_k = sdesc_sw128(sK, 16, 1024), dV_k = sdesc_sw128(sV, 16, 1024);
-      bool ok = !issuer_a || mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);
+      bool ok = role == 1 || mbar_wait(&kv_full, 0, &abort_flag, p.status, 501);  // K, V
       int it = 0;
       for (int i = qtiles.first(); ok && i < iend; i = qtiles.next(i + 1), ++it) {
         const int qs = it % C::kQStages, ds = it % C::kDOStages;
         const uint32_t sQ = sQ0 + qs * C::kTileBytes, sDO = sDO0 + ds * C::kTileBytes;
-        ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
-        if (!ok) break;
+        if (!issuer_c) {  // A and B read Q_i
+          ok = mbar_wait(&q_full[qs], (it / C::kQStages) & 1, &abort_flag, p.status, 502);
+          if (!ok) break;
+        }
         if (issuer_a) {
-          const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dDO_k = sdesc_sw128(sDO, 16, 1024);
+          const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024);
           // P^T of the previous tile sits in the S^T columns until its dV is done
           if (it > 0)
             ok = mbar_wait(&do_empty[(it - 1) % C::kDOStages], ((it - 1) / C::kDOStages) & 1,
@@ -257,6 +265,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
           }
           mma_commit(&s_ready);
+        } else if (issuer_c) {
+          const uint64_t dDO_k = sdesc_sw128(sDO, 16, 1024);
           // dS^T of the previous tile sits in the dP^T columns until its dK is done
           if (it > 0)
             ok = mbar_wait(&q_empty[(it - 1) % C::kQStages], ((it - 1) / C::kQStages) & 1,
@@ -271,6 +281,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             mma_ss(tmem + C::kColDP, dV_k + koff, dDO_k + koff, idesc_s, ks > 0);
           }
           mma_commit(&dp_ready);
+          mma_commit(&do_empty[ds]);  // this reader of dO_i is done
         } else {
           const uint64_t dQ_mn = sdesc_sw128(sQ, C::kChunkBytes, 1024);
           const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
@@ -299,9 +310,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
       // each issuer's MMAs are complete once its drain barrier flips; B's last
-      // MMA (dK) follows every MMA of A (it waited for the last dP^T through
-      // ds_ready), so `drain` alone tells the math that all are done
-      uint64_t* my_drain = issuer_a ? &drain_a : &drain;
+      // MMA (dK) follows every MMA of A and C (B's last dV waited for the last
+      // S^T through p_ready, its last dK for the last dP^T through ds_ready),
+      // so `drain` alone tells the math that all are done
+      uint64_t* my_drain = issuer_a ? &drain_a : issuer_c ? &drain_c : &drain;
       mma_commit(my_drain);
       mbar_drain(my_drain, 0);
     }
