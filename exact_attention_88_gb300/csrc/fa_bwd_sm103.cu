@@ -115,8 +115,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, s_ready, dp_ready, p_ready, ds_ready, stats_ready, drain, drain_a,
-      drain_c;
+  __shared__ uint64_t kv_full, dp_ready, ds_ready, stats_ready, drain, drain_a, drain_c;
+  // S^T is computed and consumed in two halves of 64 query columns: half h
+  // holds warpgroups 2h and 2h+1's columns, and their packed P^T.
+  //   s_ready[h]: S^T half h is in TMEM (issuer A)
+  //   p_ready[h]: P^T of half h is in TMEM (the 8 warps of warpgroups 2h, 2h+1)
+  //   s_free[h]:  dV's K steps of half h are done, so half h may be overwritten
+  //               by the next tile's S^T (issuer B)
+  __shared__ uint64_t s_ready[2], p_ready[2], s_free[2];
   // q_empty[s] completes when dK of the tile in Q stage s is done (dK is the
   // last reader of Q_i: S^T was read before the math could produce dS^T): it
   // both frees the stage and tells issuer C that dS^T (in the dP^T columns) was
@@ -145,9 +151,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&kv_full, 1);
-    mbar_init(&s_ready, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(&s_ready[h], 1);
+      mbar_init(&p_ready[h], C::kMathWarps / 2);  // one arrival per warp of the half
+      mbar_init(&s_free[h], 1);
+    }
     mbar_init(&dp_ready, 1);
-    mbar_init(&p_ready, C::kMathWarps);  // one arrival per math warp
     mbar_init(&ds_ready, C::kMathWarps);
     mbar_init(&stats_ready, 4);
     mbar_init(&drain, 1);
@@ -233,7 +242,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int role = warp - C::kMathWarps - 1;  // 0: A, 1: B, 2: C
     const bool issuer_a = role == 0, issuer_c = role == 2;
     if (lane == 0 && iend > 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);   // dP^T
+      constexpr uint32_t idesc_s64 = idesc_bf16(128, 64, false, false);  // S^T halves
       constexpr uint32_t idesc_acc = idesc_bf16(128, D, false, true);   // dV, dK
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
       const uint32_t sQ0 = smem_addr(smem + C::kOffQ), sDO0 = smem_addr(smem + C::kOffDO);
@@ -252,19 +262,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         if (issuer_a) {
           const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024);
-          // P^T of the previous tile sits in the S^T columns until its dV is done
-          if (it > 0)
-            ok = mbar_wait(&do_empty[(it - 1) % C::kDOStages], ((it - 1) / C::kDOStages) & 1,
-                           &abort_flag, p.status, 503);
-          if (!ok) break;
-          tc_fence_after();
-          // S^T = K Q^T  (K dimension = d; 16 per MMA; 4 steps per 128-byte chunk)
+          for (int h = 0; h < 2 && ok; ++h) {
+            // P^T of the previous tile's half h sits in those S^T columns until
+            // dV has read it
+            if (it > 0) ok = mbar_wait(&s_free[h], (it - 1) & 1, &abort_flag, p.status, 503);
+            if (!ok) break;
+            tc_fence_after();
+            // S^T half h = K Q^T of query rows [64h, 64h + 64): N = 64; those
+            // rows start 64 x 128 bytes into each chunk of the Q tile
+            const uint64_t dQh = dQ_k + ((uint32_t)(64 * 128 * h) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
-            mma_ss(tmem + C::kColS, dK_k + koff, dQ_k + koff, idesc_s, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t koff = ((ks >> 2) * C::kChunkBytes + (ks & 3) * 32) >> 4;
+              mma_ss(tmem + C::kColS + 64 * h, dK_k + koff, dQh + koff, idesc_s64, ks > 0);
+            }
+            mma_commit(&s_ready[h]);
           }
-          mma_commit(&s_ready);
+          if (!ok) break;
         } else if (issuer_c) {
           const uint64_t dDO_k = sdesc_sw128(sDO, 16, 1024);
           // dS^T of the previous tile sits in the dP^T columns until its dK is done
@@ -287,16 +301,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           const uint64_t dDO_mn = sdesc_sw128(sDO, C::kChunkBytes, 1024);
           const uint32_t acc = it > 0 ? 1u : 0u;
           ok = mbar_wait(&do_full[ds], (it / C::kDOStages) & 1, &abort_flag, p.status, 508);
-          if (ok) ok = mbar_wait(&p_ready, it & 1, &abort_flag, p.status, 505);
-          if (!ok) break;
-          tc_fence_after();
-          // dV += P^T dO (P^T in TMEM: warpgroup w's 32 query columns sit packed in
-          // columns [32w, 32w+16) of the S^T region)
+          // dV += P^T dO, half by half as each half's P^T lands (P^T in TMEM:
+          // warpgroup w's 32 query columns sit packed in columns [32w, 32w+16)
+          // of the S^T region; half h = K steps 4h .. 4h + 3)
+          for (int h = 0; h < 2 && ok; ++h) {
+            ok = mbar_wait(&p_ready[h], it & 1, &abort_flag, p.status, 505);
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
-                   dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
-          mma_commit(&do_empty[ds]);
+            for (int k4 = 0; k4 < 4; ++k4) {
+              const int ks = 4 * h + k4;
+              mma_ts(tmem + C::kColDV, tmem + C::kColS + 32 * (ks >> 1) + 8 * (ks & 1),
+                     dDO_mn + ks * (2048 >> 4), idesc_acc, acc | (ks > 0));
+            }
+            mma_commit(&s_free[h]);
+          }
+          if (!ok) break;
+          mma_commit(&do_empty[ds]);  // this reader of dO_i is done
           ok = mbar_wait(&ds_ready, it & 1, &abort_flag, p.status, 507);
           if (!ok) break;
           tc_fence_after();
@@ -311,7 +332,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       // each issuer's MMAs are complete once its drain barrier flips; B's last
       // MMA (dK) follows every MMA of A and C (B's last dV waited for the last
-      // S^T through p_ready, its last dK for the last dP^T through ds_ready),
+      // S^T halves through p_ready, its last dK for the last dP^T through ds_ready),
       // so `drain` alone tells the math that all are done
       uint64_t* my_drain = issuer_a ? &drain_a : issuer_c ? &drain_c : &drain;
       mma_commit(my_drain);
@@ -382,7 +403,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           pf[c] = (key < p.N && qr0 + c < p.N) ? __ldg(bcol + (long long)c * p.lb.n) * kLog2e : 0.f;
       }
       ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
-      if (ok) ok = mbar_wait_warp(&s_ready, it & 1, &abort_flag, p.status, 602);
+      if (ok) ok = mbar_wait_warp(&s_ready[wg >> 1], it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
       const int q0 = i * 128;
@@ -428,7 +449,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(&p_ready);
+      mbar_arrive_warp(&p_ready[wg >> 1]);
       // dropout: the next tile's keep bits, drawn while dP^T is computed
       if (kExtra && p.drop.t) {
         const int inext = qtiles.next(i + 1);
