@@ -38,6 +38,8 @@ CASES = [
     (2, 3, 384, 64, False, "padding", 0.2),
     (1, 2, 520, 128, True, "sparse", 0.3),
     (1, 1, 1000, 128, True, "none", 0.9),
+    (1, 1, 1, 64, False, "none", 0.5),          # one token
+    (2, 2, 200, 128, False, "padding0", 0.3),   # a batch element whose keys are all padding
 ]
 
 
@@ -47,6 +49,8 @@ def _case(B, H, N, d, mask, seed):
     if mask == "padding":
         kv = rng.integers(1, N + 1, B)
         kv[0] = min(N, 100)
+    if mask == "padding0":
+        kv = np.array([0] + [N] * (B - 1))
     if mask == "sparse":
         T = (N + 127) // 128
         bm = (rng.random((T, T)) < 0.4).astype(np.uint8)
