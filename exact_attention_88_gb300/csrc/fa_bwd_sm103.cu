@@ -14,15 +14,17 @@
 //   [2d, 2d+128)    S^T = K_j Q_i^T, then P^T (bf16, packed two per column:
 //                   warpgroup w's 32 query columns in [32w, 32w+16))
 //   [2d+128, +128)  dP^T = V_j dO_i^T, then dS^T (packed the same way)
-// Per query tile, in tensor-core order, with the math overlapping:
-//   S^T            both operands K-major in shared memory (after the previous
-//                  dV, the last reader of P^T)
-//   dP^T           (after the previous dK, the last reader of dS^T; meanwhile
-//                  the math computes P^T = 2^(c S^T - lse2_i) into TMEM)
-//   dV += P^T dO_i A from TMEM (meanwhile the math computes
-//                  dS^T = scale P^T o (dP^T - D_i) into TMEM)
+// Per query tile, with the math overlapping:
+//   S^T            in two halves of 64 query columns (N = 64), both operands
+//                  K-major in shared memory; half h after the previous tile's
+//                  dV steps of half h, the readers of the P^T packed there
+//   dP^T           after the previous dK, the last reader of dS^T (meanwhile
+//                  the math computes P^T = 2^(c S^T - lse2_i) into TMEM, each
+//                  half as soon as its S^T half is in)
+//   dV += P^T dO_i A from TMEM, half by half as each half's P^T lands
+//                  (meanwhile the math computes dS^T = scale P^T o (dP^T - D_i))
 //   dK += dS^T Q_i A from TMEM
-// so the next tile's S^T queues behind dK without waiting for it.
+// so that a tile's S^T half waits for one half of the previous dV only.
 //
 // Roles (640 threads): warps 0-15 are four math warpgroups -- warpgroup w owns
 // query columns [32w, 32w+32) of S^T / dP^T and d columns [w d/4, (w+1) d/4)
