@@ -39,7 +39,7 @@ DEFAULT_WORKLOAD = "long_causal_d128"
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # current version of that kernel; set to None whenever the kernel changes
 # until it is captured again.
-DKDV_DRAM_BYTES = {"long_causal_d128": 376423424 + 103657984}
+DKDV_DRAM_BYTES = {"long_causal_d128": 379537664 + 103406336}
 
 
 def measured_peaks():
@@ -427,9 +427,11 @@ def host_cores():
 def oracle_sample(w, case, n_rows):
     """Time the oracle on the last n_rows query rows of head (0, 0) (the rows
     that see the most keys under a causal mask): O, lse, dQ of those rows and
-    their dK, dV contributions.  Returns (seconds, algorithmic FLOPs of the
-    sample under the benchmark's convention)."""
+    their dK, dV contributions; all N rows when the sequence is shorter.
+    Returns (seconds, algorithmic FLOPs of the sample under the benchmark's
+    convention, rows timed)."""
     import oracle
+    n_rows = max(1, min(n_rows, w.N))
     rows = np.arange(w.N - n_rows, w.N)
     kw = dict(causal=w.causal, kv_len=case["kv_len"], block_mask=case["block_mask"])
     t0 = time.perf_counter()
@@ -440,11 +442,11 @@ def oracle_sample(w, case, n_rows):
                          None if case["kv_len"] is None else int(case["kv_len"][0]),
                          case["block_mask"], w.block)
     fwd = 4.0 * w.d * float(vis.sum())   # Q K^T and P V over the visible pairs
-    return sec, 3.5 * fwd
+    return sec, 3.5 * fwd, n_rows
 
 
 def cpu_baseline(w, case, n_rows):
-    sec, fl = oracle_sample(w, case, n_rows)
+    sec, fl, n_rows = oracle_sample(w, case, n_rows)
     return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
             "kind": "oracle",
             "sample": "fp64 numpy oracle, fwd+bwd of the last %d query rows of head (0,0) of %s "
@@ -458,12 +460,12 @@ def run_reference(args, rank):
         return None
     w = WORKLOADS[args.workload]
     case = generate(w, seed=0, samples=1)
-    n_rows = args.reference_rows
+    n_rows = min(args.reference_rows, w.N)
     for _ in range(args.warmup):
         oracle_sample(w, case, n_rows)
     secs, fl = 0.0, 0.0
     for _ in range(args.steps):
-        s, f = oracle_sample(w, case, n_rows)
+        s, f, _ = oracle_sample(w, case, n_rows)
         secs += s
         fl += f
     value = fl / secs / 1e12

@@ -20,6 +20,7 @@ namespace fa {
 constexpr int kStatusTimeout = 6;  // equals FA_ERR_TIMEOUT
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;     // 2 s per wait
 constexpr uint64_t kDrainTimeoutNs = 500000000ull;     // 0.5 s while tearing down
+constexpr uint32_t kSuspendHintNs = 200000u;           // longest sleep of one wait attempt
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -65,6 +66,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with a suspend-time hint: a thread whose phase has not completed
+// sleeps until it completes (or the hint runs out) instead of polling, so a
+// waiting warp leaves the issue slots of its SMSP to the warps that work.
+__device__ __forceinline__ bool mbar_try_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
 
 // Wait until the phase with the given parity of `bar` has completed.  Gives up
 // (returns false) when another role has already aborted, or after
@@ -79,7 +93,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
 #pragma unroll 1
     for (int i = 0; i < 16; ++i)
-      if (mbar_try(a, parity)) return true;
+      if (mbar_try_sleep(a, parity)) return true;
     if (*abort_flag) return false;
     if (global_timer() - t0 > limit_ns) {
       *abort_flag = 1;

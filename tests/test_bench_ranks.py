@@ -59,3 +59,17 @@ def test_reference_arm_does_no_work_off_rank_0():
         warmup = 0
         reference_rows = 8
     assert bench.run_reference(Args(), rank=1) is None
+
+
+def test_cpu_sample_is_clamped_to_the_sequence():
+    """A sample of more query rows than the sequence has times all N rows
+    (it once indexed rows before the start of the sequence)."""
+    from workloads import WORKLOADS, generate
+    w = WORKLOADS["tiny_fp32_causal"]
+    case = generate(w, seed=0, samples=1)
+    sec, fl, n = bench.oracle_sample(w, case, 8192)
+    assert n == w.N and sec > 0
+    # causal: N (N + 1) / 2 visible pairs, 3.5 x (4 d) FLOPs per pair
+    assert fl == pytest.approx(3.5 * 4 * w.d * w.N * (w.N + 1) / 2)
+    res = bench.cpu_baseline(w, case, 8192)
+    assert "last %d query rows" % w.N in res["sample"] and res["value"] > 0
