@@ -117,7 +117,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t kv_full, dp_ready, ds_ready, stats_ready, drain, drain_a, drain_c;
+  __shared__ uint64_t kv_full, dp_ready, ds_ready, drain, drain_a, drain_c;
+  // The copy of the statistics is split by warpgroup: warpgroup w reads only
+  // entries [32w, 32w+32), its query columns.  stats_read[w] completes when its
+  // four warps are past their last read of the tile's entries (their dS^T),
+  // stats_ready[w] when its first warp has written the next tile's.
+  __shared__ uint64_t stats_read[4], stats_ready[4];
   // S^T is computed and consumed in two halves of 64 query columns: half h
   // holds warpgroups 2h and 2h+1's columns, and their packed P^T.
   //   s_ready[h]: S^T half h is in TMEM (issuer A)
@@ -160,7 +165,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     mbar_init(&dp_ready, 1);
     mbar_init(&ds_ready, C::kMathWarps);
-    mbar_init(&stats_ready, 4);
+    for (int w = 0; w < 4; ++w) {
+      mbar_init(&stats_read[w], 4);
+      mbar_init(&stats_ready[w], 1);
+    }
     mbar_init(&drain, 1);
     mbar_init(&drain_a, 1);
     mbar_init(&drain_c, 1);
@@ -354,15 +362,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const bool bias_on = kExtra && p.bias != nullptr;
     int it = 0;
     bool ok = true;
-    // Statistics of one query row: loaded raw (lse, D) by a thread of the
-    // first warpgroup, converted to what the math uses (-lse2, -D) only when
-    // stored, so that the load's latency is not waited for before then.
+    // Statistics of one query row: loaded raw (lse, D) by a lane of the
+    // warpgroup's first warp (lane l: query column col0 + l), converted to
+    // what the math uses (-lse2, -D) only when stored, so that the load's
+    // latency is not waited for before then.
+    const bool stats_writer = (warp & 3) == 0;
     struct RowStats {
       float nl2, nd;
     };
     auto load_stats = [&](int qt) {
       RowStats st{-INFINITY, 0.f};  // rows past the end: P = 0
-      const int q = qt * 128 + tid;
+      const int q = qt * 128 + col0 + lane;
       if (qt < iend && q < p.N) {
         st.nl2 = p.lse[head_row0 + q];
         st.nd = p.Dvec[head_row0 + q];
@@ -380,17 +390,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint32_t keep_next = ~0u;
     if (kExtra && p.drop.t && iend > 0)
       keep_next = keep_bits_of_key(p.drop, (uint32_t)bh, key, qtiles.first() * 128 + col0);
-    if (tid < 128 && iend > 0) {
+    if (stats_writer && iend > 0) {
       const RowStats st = finish_stats(load_stats(qtiles.first()));
-      s_nl2[tid] = st.nl2;
-      s_nD[tid] = st.nd;
-      mbar_arrive_warp(&stats_ready);
+      s_nl2[col0 + lane] = st.nl2;
+      s_nD[col0 + lane] = st.nd;
+      mbar_arrive_warp(&stats_ready[wg]);
     }
     for (int i = qtiles.first(); i < iend; i = qtiles.next(i + 1), ++it) {
-      // ---- the next tile's statistics: loaded now, stored once every math
-      // thread is past this tile's dS (the loads' latency hides behind the MMAs)
+      // ---- the next tile's statistics: loaded now, stored once the
+      // warpgroup's threads are past this tile's dS (the loads' latency hides
+      // behind the MMAs)
       RowStats next_st{};
-      if (tid < 128) next_st = load_stats(qtiles.next(i + 1));
+      if (stats_writer) next_st = load_stats(qtiles.next(i + 1));
       // dropout: keep bits of this key for the warpgroup's 32 query rows (all
       // set without dropout), drawn during the previous tile; bias:
       // bias[query][key] times log2(e) of those rows, in pf, read while S^T is
@@ -404,7 +415,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int c = 0; c < 32; ++c)
           pf[c] = (key < p.N && qr0 + c < p.N) ? __ldg(bcol + (long long)c * p.lb.n) * kLog2e : 0.f;
       }
-      ok = mbar_wait_warp(&stats_ready, it & 1, &abort_flag, p.status, 601);
+      ok = mbar_wait_warp(&stats_ready[wg], it & 1, &abort_flag, p.status, 601);
       if (ok) ok = mbar_wait_warp(&s_ready[wg >> 1], it & 1, &abort_flag, p.status, 602);
       if (!ok) break;
       tc_fence_after();
@@ -498,14 +509,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&ds_ready);
-      // ---- the next tile's statistics replace this tile's once every math
-      // thread is past its last read of them (ds_ready complete)
-      if (tid < 128) {
-        if (!mbar_wait_warp(&ds_ready, it & 1, &abort_flag, p.status, 600)) break;
+      mbar_arrive_warp(&stats_read[wg]);
+      // ---- the next tile's statistics replace this tile's once the
+      // warpgroup's four warps are past their last read of them
+      if (stats_writer) {
+        if (!mbar_wait_warp(&stats_read[wg], it & 1, &abort_flag, p.status, 600)) break;
         const RowStats st = finish_stats(next_st);
-        s_nl2[tid] = st.nl2;
-        s_nD[tid] = st.nd;
-        mbar_arrive_warp(&stats_ready);
+        s_nl2[col0 + lane] = st.nl2;
+        s_nD[col0 + lane] = st.nd;
+        mbar_arrive_warp(&stats_ready[wg]);
       }
     }
     // ------------------------------------------------------------ dK, dV out
