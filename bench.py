@@ -39,7 +39,7 @@ DEFAULT_WORKLOAD = "long_causal_d128"
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # current version of that kernel; set to None whenever the kernel changes
 # until it is captured again.
-DKDV_DRAM_BYTES = {"long_causal_d128": None}
+DKDV_DRAM_BYTES = {"long_causal_d128": 380852480 + 103521280}
 
 
 def measured_peaks():
