@@ -67,9 +67,13 @@ def test_cpu_sample_is_clamped_to_the_sequence():
     from workloads import WORKLOADS, generate
     w = WORKLOADS["tiny_fp32_causal"]
     case = generate(w, seed=0, samples=1)
-    sec, fl, n = bench.oracle_sample(w, case, 8192)
-    assert n == w.N and sec > 0
+    sec, fl, n, slices = bench.oracle_sample(w, case, 8192)
+    assert n == w.N and slices == 1 and sec > 0
     # causal: N (N + 1) / 2 visible pairs, 3.5 x (4 d) FLOPs per pair
     assert fl == pytest.approx(3.5 * 4 * w.d * w.N * (w.N + 1) / 2)
-    res = bench.cpu_baseline(w, case, 8192)
-    assert "last %d query rows" % w.N in res["sample"] and res["value"] > 0
+    # several slices: the work adds up; more slices than the workload has are capped
+    _, fl2, _, slices2 = bench.oracle_sample(w, case, 8192, heads=5)
+    assert slices2 == w.B * w.H and fl2 == pytest.approx(slices2 * fl)
+    res = bench.cpu_baseline(w, case, 8192, 2)
+    assert "last %d query rows of each of the first 2" % w.N in res["sample"]
+    assert res["value"] > 0

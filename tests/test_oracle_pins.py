@@ -307,6 +307,19 @@ def test_dk_sums_to_zero(kind):
     assert np.max(np.abs(tot)) <= 1e-10 * max(1.0, np.linalg.norm(dk))
 
 
+@pytest.mark.parametrize("kind", MASKS)
+def test_dv_sums_to_the_summed_do(kind):
+    """Every row of P sums to one and dV = P^T dO, so the value gradients of a
+    head sum to its dO summed over the rows (every row here sees a key).  A
+    transposed P in dV, or a dropped row, breaks it."""
+    B, H, N, d = 2, 2, 40, 8
+    q, k, v, do = (rand((B, H, N, d), 70 + i) for i in range(4))
+    ma = mask_args(kind, B, N, 65, block=8)
+    _, _, dv, _ = A.backward(q, k, v, do, 0.3, **ma)
+    err = np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2)))
+    assert err <= 1e-10 * max(1.0, np.linalg.norm(dv))
+
+
 # ---------------------------------------------------------------------------
 # 11. hand-derived values
 # ---------------------------------------------------------------------------

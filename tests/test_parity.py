@@ -170,6 +170,11 @@ def test_workload_sampled(fa, name):
     tot = np.linalg.norm(dk64.sum(axis=2), axis=-1)
     per = np.linalg.norm(dk64, axis=(2, 3))
     assert np.all(tot <= 2e-2 * per)
+    # any size: every row sees a key and its probabilities sum to one, so the
+    # value gradients of each head sum to its dO summed over the rows
+    dv64 = f64(dv)
+    err = np.linalg.norm(dv64.sum(axis=2) - case["do"].sum(axis=2), axis=-1)
+    assert np.all(err <= 2e-2 * np.linalg.norm(dv64, axis=(2, 3)))
 
 
 @pytest.mark.parametrize("pattern", ["local", "local_global", "strided", "butterfly"])
