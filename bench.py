@@ -60,7 +60,114 @@ def kept_fraction(block_mask):
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 
+NVML_CLOCK_SM = 1
+# clock event reason bits of NVML that the timing rules look at
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def load_nvml():
+    """The driver's NVML library, or None."""
+    import ctypes
+    for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            pass
+    return None
+
+
+class NvmlSampler:
+    """Polls one GPU's SM clock, clock event reasons and power through NVML
+    (read-only queries) from a host thread every `period_s`; stop(t0, t1)
+    summarises the samples whose host time (time.perf_counter) lies in
+    [t0, t1], the timed region.  A timed region of a few tens of ms still gets
+    dozens of samples, where nvidia-smi's loop would give one or none."""
+
+    def __init__(self, uuid=None, index=0, lib=None, period_s=0.001):
+        self.uuid, self.index, self.lib, self.period_s = uuid, index, lib, period_s
+        self.samples = []
+        self.max_mhz = None
+        self.thread = None
+        self.done = threading.Event()
+
+    def start(self):
+        """True when NVML answered and polling has started."""
+        import ctypes
+        lib = self.lib
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = bool(self.uuid) and lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(),
+                                                               ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) == 0
+        if not ok:
+            lib.nvmlShutdown()
+            return False
+        self.handle = h
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(NVML_CLOCK_SM), ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self.reasons_fn = None
+        for name in ("nvmlDeviceGetCurrentClocksEventReasons",
+                     "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            try:
+                self.reasons_fn = getattr(lib, name)
+                break
+            except AttributeError:
+                pass
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        return True
+
+    def _poll(self):
+        import ctypes
+        lib, h = self.lib, self.handle
+        while not self.done.is_set():
+            t = time.perf_counter()
+            sm, rs, pw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+            a = lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(NVML_CLOCK_SM), ctypes.byref(sm))
+            b = self.reasons_fn(h, ctypes.byref(rs)) if self.reasons_fn is not None else -1
+            c = lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            self.samples.append((t, float(sm.value) if a == 0 else None,
+                                 int(rs.value) if b == 0 else None,
+                                 pw.value / 1000.0 if c == 0 else None))
+            time.sleep(self.period_s)
+
+    def stop(self, t0, t1):
+        self.done.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+            self.lib.nvmlShutdown()
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        sm = [x[1] for x in inside if x[1] is not None]
+        power = [x[3] for x in inside if x[3] is not None]
+        reasons, bits = set(), 0
+        for x in inside:
+            if x[2] is not None:
+                bits |= x[2]
+                reasons.update(n for bit, n in NVML_REASONS.items() if x[2] & bit)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_min_mhz": min(sm) if sm else None, "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons),
+                "reason_bits_seen": hex(bits), "samples": len(sm),
+                "source": "NVML polled every %g ms from the host; samples inside the timed "
+                          "region only" % (1e3 * self.period_s)}
+
+
+def device_uuid(dev):
+    """NVML's name of a torch CUDA device ("GPU-..."), or None."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 class ClockSampler:
+    """nvidia-smi's query loop: the fallback when NVML cannot be loaded."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -228,23 +335,28 @@ def run_gpu(args, rank, world, local_rank):
     if code != 0:
         raise RuntimeError("device status %d at site %d during warm-up" % (code, site))
 
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
+    sampler = NvmlSampler(device_uuid(dev), local_rank, load_nvml())
+    fallback = None
+    if not sampler.start():
+        fallback = ClockSampler(local_rank)
+        fallback.start()
+        time.sleep(0.3)
     barrier()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    host_t0 = time.perf_counter()
     t0.record(stream)
     for _ in range(args.steps):
         step(False)
     t1.record(stream)
     barrier()
+    host_t1 = time.perf_counter()
     elapsed_ms = t0.elapsed_time(t1)
     # per-kernel pass: CUDA events on the launching stream around each launch
     for _ in range(args.steps):
         step(True)
     barrier()
-    clocks = sampler.stop()
+    clocks = fallback.stop() if fallback is not None else sampler.stop(host_t0, host_t1)
     code, site = fa.fa_get_device_status(stream)
     if code != 0:
         raise RuntimeError("device status %d at site %d in the timed region" % (code, site))
