@@ -81,6 +81,11 @@ def fwd(fa, **kw):
     (dict(causal=2), 1), (dict(scale=0.0), 1), (dict(scale=-1.0), 1),
     (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
     (dict(q=FAKE + 8), 3), (dict(o=FAKE + 2), 3), (dict(lse=FAKE + 2), 3),
+    # the size limits, on both sides: B*H <= 65535, B*H*N*d <= 2^40 elements
+    # (5 = FA_ERR_CUDA: the arguments passed, and the launch found no GPU here)
+    (dict(B=257, H=255), 5), (dict(B=65535), 5), (dict(B=65536), 2), (dict(B=256, H=256), 2),
+    (dict(B=1024, N=1 << 24, d=64), 5),          # exactly 2^40 elements
+    (dict(B=1024, N=(1 << 24) + 1, d=64), 2),
 ])
 def test_fwd_rejects_bad_arguments(fa, kw, code):
     assert fwd(fa, **kw) == code
