@@ -143,3 +143,39 @@ def test_everything_together(fa):
     assert max_abs(lse.cpu().numpy().astype(np.float64), rl, finite_only=True) <= tl
     for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), (rdq, rdk, rdv)):
         assert rel_fro(f64(g), r) <= tg, name
+
+
+def test_every_option_at_once_on_strided_layouts(fa):
+    """Q, K, V, dO (and so O and the gradients) as [B, N, H, d] buffers seen
+    through [B, H, N, d] views, a per-head bias, dropout, the causal mask and
+    key padding, all in one call, against the oracle on the same values."""
+    B, H, N, d, p, seed, offset = 2, 3, 300, 64, 0.2, 4242, 9
+    rng = np.random.default_rng(77)
+    kv = rng.integers(1, N + 1, B)
+    case = random_case(B, H, N, d, seed=78, kv_len=kv)
+    t = to_device(case, "bf16")
+    views = {}
+    for n in ("q", "k", "v", "do"):
+        buf = torch.empty((B, N, H, d), dtype=torch.bfloat16, device="cuda")
+        views[n] = buf.transpose(1, 2)
+        views[n].copy_(t[n])
+    bias_np = rng.standard_normal((1, H, N, N)).astype(np.float32)
+    bias = torch.from_numpy(bias_np).cuda()
+    scale = d ** -0.5
+    kw = dict(kv_len=t["kv_len"], bias=bias, dropout_p=p, seed=seed, offset=offset)
+    o, lse = fa.forward(views["q"], views["k"], views["v"], scale, True, **kw)
+    assert o.stride() == views["q"].stride()
+    dq, dk, dv = fa.backward(views["q"], views["k"], views["v"], o, views["do"], lse, scale,
+                             True, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_status()[0] == 0
+    okw = dict(causal=True, kv_len=kv, bias=bias_np.astype(np.float64),
+               dropout=(p, seed, offset))
+    ro, rl = oracle.forward(case["q"], case["k"], case["v"], scale, **okw)
+    rdq, rdk, rdv, _ = oracle.backward(case["q"], case["k"], case["v"], case["do"], scale, **okw)
+    to, tl, tg = TOL["bf16"]
+    assert max_abs(f64(o), ro) <= to * D.keep_scale(p), "O"
+    assert max_abs(lse.cpu().numpy().astype(np.float64), rl, finite_only=True) <= tl, "lse"
+    for name, g, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), (rdq, rdk, rdv)):
+        e = rel_fro(f64(g), r)
+        assert e <= tg, (name, e)
