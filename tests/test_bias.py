@@ -145,10 +145,11 @@ def test_everything_together(fa):
         assert rel_fro(f64(g), r) <= tg, name
 
 
-def test_every_option_at_once_on_strided_layouts(fa):
-    """Q, K, V, dO (and so O and the gradients) as [B, N, H, d] buffers seen
-    through [B, H, N, d] views, a per-head bias, dropout, the causal mask and
-    key padding, all in one call, against the oracle on the same values."""
+def test_everything_together_d64(fa):
+    """The d = 64 kernels with every option at once, as the test above does for
+    d = 128: Q, K, V, dO (and so O and the gradients) as [B, N, H, d] buffers
+    seen through [B, H, N, d] views, a per-head bias, dropout, the causal mask
+    and key padding, against the oracle on the same values."""
     B, H, N, d, p, seed, offset = 2, 3, 300, 64, 0.2, 4242, 9
     rng = np.random.default_rng(77)
     kv = rng.integers(1, N + 1, B)
