@@ -77,3 +77,22 @@ def test_cpu_sample_is_clamped_to_the_sequence():
     res = bench.cpu_baseline(w, case, 8192, 2)
     assert "last %d query rows of each of the first 2" % w.N in res["sample"]
     assert res["value"] > 0
+
+
+def test_reference_arm_line_on_rank_0():
+    """The reference arm's line: the oracle's throughput with the keys of the
+    GPU arm's line, a cpu_baseline describing the run, and an e2e equal to
+    the value with no host-device bytes."""
+    class Args:
+        workload = "tiny_fp32_causal"
+        steps = 2
+        warmup = 1
+        reference_rows = 64
+    res = bench.run_reference(Args(), rank=0)
+    assert res["impl"] == "reference" and res["value"] > 0 and res["dtype"] == "f64"
+    assert res["steps"] == 2 and res["warmup"] == 1 and res["higher_is_better"] is True
+    assert res["config"]["workload"] == "tiny_fp32_causal"
+    cpu = res["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["value"] == res["value"] and cpu["cores"] >= 1
+    assert res["e2e"] == {"value": res["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}
