@@ -88,6 +88,7 @@ class NvmlSampler:
         self.uuid, self.index, self.lib, self.period_s = uuid, index, lib, period_s
         self.samples = []
         self.max_mhz = None
+        self.driver = None
         self.thread = None
         self.done = threading.Event()
 
@@ -106,6 +107,12 @@ class NvmlSampler:
             lib.nvmlShutdown()
             return False
         self.handle = h
+        try:
+            buf = ctypes.create_string_buffer(96)
+            if lib.nvmlSystemGetDriverVersion(buf, ctypes.c_uint(96)) == 0:
+                self.driver = buf.value.decode(errors="replace")
+        except (AttributeError, ctypes.ArgumentError, OSError, ValueError):
+            pass  # a report field must not end the run
         mx = ctypes.c_uint()
         if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(NVML_CLOCK_SM), ctypes.byref(mx)) == 0:
             self.max_mhz = float(mx.value)
@@ -164,6 +171,17 @@ def device_uuid(dev):
     except (AttributeError, RuntimeError):
         return None
     return u if u.startswith("GPU-") else "GPU-" + u
+
+
+def device_info(dev, driver):
+    """The GPU's name, the driver version (from NVML, or None) and the CUDA
+    runtime torch was built with; never raises."""
+    import torch
+    try:
+        name = torch.cuda.get_device_name(dev)
+    except Exception:  # noqa: BLE001  (a report field must not end the run)
+        name = None
+    return {"name": name, "driver": driver, "cuda_runtime": torch.version.cuda}
 
 
 class ClockSampler:
@@ -420,6 +438,7 @@ def run_gpu(args, rank, world, local_rank):
                         "flops_per_launch": dq_flops},
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
+        "device": device_info(dev, sampler.driver),
     }
     if kept is not None:
         result["dense_equivalent"] = {

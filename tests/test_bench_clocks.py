@@ -62,6 +62,12 @@ class FakeNvml:
         return 0
 
 
+class FakeNvmlWithDriver(FakeNvml):
+    def nvmlSystemGetDriverVersion(self, buf, length):
+        buf.value = b"580.159"
+        return 0
+
+
 def _run(lib, uuid):
     a = time.perf_counter() + 0.02
     lib.hot0, lib.hot1 = a, a + 0.08
@@ -87,6 +93,18 @@ def test_device_found_by_index_when_the_uuid_is_unknown():
     lib = FakeNvml(0, 0, uuid=b"GPU-other")
     res = _run(lib, "GPU-fake")
     assert lib.handles == ["index"] and res["sm_mhz"] == 1980.0
+
+
+def test_driver_version_when_nvml_has_it():
+    lib = FakeNvmlWithDriver(0, 0)
+    s = bench.NvmlSampler("GPU-fake", 0, lib)
+    assert s.start()
+    s.stop(0.0, 0.0)
+    assert s.driver == "580.159"
+    s = bench.NvmlSampler("GPU-fake", 0, FakeNvml(0, 0))   # no such call: no version
+    assert s.start()
+    s.stop(0.0, 0.0)
+    assert s.driver is None
 
 
 def test_missing_nvml_is_reported_not_raised():
