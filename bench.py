@@ -67,7 +67,7 @@ NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowd
 
 
 def load_nvml():
-    """The driver's NVML library, or None."""
+    """NVML (the library that ships with the NVIDIA driver), or None."""
     import ctypes
     for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
         try:
@@ -174,7 +174,7 @@ def device_uuid(dev):
 
 
 def device_info(dev, driver):
-    """The GPU's name, the driver version (from NVML, or None) and the CUDA
+    """The GPU's name, the NVIDIA driver version (from NVML, or None) and the CUDA
     runtime torch was built with; never raises."""
     import torch
     try:
