@@ -469,3 +469,132 @@ def test_row_blocks_sum_to_full_backward(kind):
             dv_sum += dvp
         assert np.max(np.abs(dk_sum - dk[b, 0])) <= 1e-12
         assert np.max(np.abs(dv_sum - dv[b, 0])) <= 1e-12
+
+
+# ---------------------------------------------------------------------------
+# 15. mask orientation and boundaries, pinned without the oracle's own
+#     visibility function: the expected visibility is written out by hand and
+#     the attention and its derivative are computed with scalar loops.
+# ---------------------------------------------------------------------------
+
+def _brute_backward(q, k, v, do, s, vis):
+    """dQ, dK, dV of L = sum(O o dO) with scalar loops over an explicit
+    visibility table (the textbook derivative of the definition)."""
+    n, d = len(q), len(q[0])
+    p = [[0.0] * n for _ in range(n)]
+    for i in range(n):
+        idx = [j for j in range(n) if vis[i][j]]
+        if not idx:
+            continue
+        logit = {j: s * sum(q[i][c] * k[j][c] for c in range(d)) for j in idx}
+        mx = max(logit.values())
+        tot = sum(math.exp(x - mx) for x in logit.values())
+        for j in idx:
+            p[i][j] = math.exp(logit[j] - mx) / tot
+    dp = [[sum(do[i][c] * v[j][c] for c in range(d)) for j in range(n)] for i in range(n)]
+    drow = [sum(p[i][j] * dp[i][j] for j in range(n)) for i in range(n)]
+    ds = [[p[i][j] * (dp[i][j] - drow[i]) for j in range(n)] for i in range(n)]
+    dq = [[s * sum(ds[i][j] * k[j][c] for j in range(n)) for c in range(d)] for i in range(n)]
+    dk = [[s * sum(ds[i][j] * q[i][c] for i in range(n)) for c in range(d)] for j in range(n)]
+    dv = [[sum(p[i][j] * do[i][c] for i in range(n)) for c in range(d)] for j in range(n)]
+    return np.array(dq), np.array(dk), np.array(dv)
+
+
+# An asymmetric tile mask (query tile i, key tile j): query tile 0 sees key
+# tile 0; query tile 1 sees key tiles 0 and 1; query tile 2 sees key tiles 1
+# and 2.  Its transpose differs in four places.
+_TILE_MASK = np.array([[1, 0, 0],
+                       [1, 1, 0],
+                       [0, 1, 1]], np.uint8)
+_TILE = 4
+_TILE_VIS = [  # 12 x 12 by hand: row i lists the keys query i sees
+    [1] * 4 + [0] * 8,
+] * 4 + [
+    [1] * 8 + [0] * 4,
+] * 4 + [
+    [0] * 4 + [1] * 8,
+] * 4
+
+
+def _tile_mask_error(A_):
+    """Largest error of the oracle module A_ against the hand-written
+    visibility: O, lse and the three gradients, block-sparse with the
+    asymmetric tile mask."""
+    N, d, s = 12, 3, 0.8
+    q, k, v, do = (rand((1, 1, N, d), 140 + i) for i in range(4))
+    o, lse = A_.forward(q, k, v, s, block_mask=_TILE_MASK, block=_TILE)
+    dq, dk, dv, _ = A_.backward(q, k, v, do, s, block_mask=_TILE_MASK, block=_TILE)
+    L = lambda x: x[0, 0].tolist()
+    ob, lb = _brute(L(q), L(k), L(v), s, _TILE_VIS)
+    gb = _brute_backward(L(q), L(k), L(v), L(do), s, _TILE_VIS)
+    errs = [np.max(np.abs(o[0, 0] - ob)), np.max(np.abs(lse[0, 0] - lb))]
+    errs += [np.max(np.abs(g[0, 0] - r)) for g, r in zip((dq, dk, dv), gb)]
+    return max(errs)
+
+
+def test_block_mask_orientation_against_hand_written_visibility():
+    """The tile mask is indexed by (query tile, key tile), as the summary
+    page's block-sparse extension states it ("Extension: block-sparse
+    FlashAttention"): checked against a visibility table typed out by hand,
+    through loops that never call the oracle's mask code."""
+    assert _tile_mask_error(A) <= 1e-12
+    # key tile 2 is seen by query tile 2 only: dK, dV of keys 8..11 come from
+    # rows 8..11 alone; key tile 0 from rows 0..7
+    N, d = 12, 3
+    q, k, v, do = (rand((1, 1, N, d), 140 + i) for i in range(4))
+    _, dk, dv, _ = A.backward(q, k, v, do, 0.8, block_mask=_TILE_MASK, block=_TILE)
+    do_cut = do.copy()
+    do_cut[0, 0, :8] = 0.0   # rows 0..7 stop contributing
+    _, dk2, dv2, _ = A.backward(q, k, v, do_cut, 0.8, block_mask=_TILE_MASK, block=_TILE)
+    assert np.array_equal(dv[0, 0, 8:], dv2[0, 0, 8:])
+    assert np.array_equal(dk[0, 0, 8:], dk2[0, 0, 8:])
+    assert np.all(dv2[0, 0, :4] == 0.0)
+
+
+def _planted(monkeypatch, mistake):
+    """A copy of the oracle's visibility function with one mistake planted in
+    it, installed for the rest of the test."""
+    real = A.visible
+
+    def wrong(rows, n_keys, causal=False, kv_len_b=None, block_mask=None, block=128, keys=None):
+        if mistake == "transposed_tile_mask" and block_mask is not None:
+            block_mask = np.asarray(block_mask).T
+        if mistake == "padding_off_by_one" and kv_len_b is not None:
+            kv_len_b = int(kv_len_b) + 1
+        return real(rows, n_keys, causal, kv_len_b, block_mask, block, keys)
+
+    monkeypatch.setattr(A, "visible", wrong)
+
+
+def test_tile_mask_pin_catches_a_transposed_mask(monkeypatch):
+    _planted(monkeypatch, "transposed_tile_mask")
+    assert _tile_mask_error(A) > 1e-2
+
+
+def _padding_error(A_):
+    """Key padding at its boundary: with kv_len = 5, key 4 is the last visible
+    key and key 5 the first hidden one.  Checked against a table typed out
+    by hand (j < 5) with scalar loops."""
+    N, d, s, L_b = 9, 3, 0.7, 5
+    q, k, v, do = (rand((1, 1, N, d), 150 + i) for i in range(4))
+    o, lse = A_.forward(q, k, v, s, kv_len=np.array([L_b]))
+    dq, dk, dv, _ = A_.backward(q, k, v, do, s, kv_len=np.array([L_b]))
+    vis = [[1] * 5 + [0] * 4 for _ in range(N)]
+    L = lambda x: x[0, 0].tolist()
+    ob, lb = _brute(L(q), L(k), L(v), s, vis)
+    gb = _brute_backward(L(q), L(k), L(v), L(do), s, vis)
+    errs = [np.max(np.abs(o[0, 0] - ob)), np.max(np.abs(lse[0, 0] - lb))]
+    errs += [np.max(np.abs(g[0, 0] - r)) for g, r in zip((dq, dk, dv), gb)]
+    return max(errs), dk, dv
+
+
+def test_key_padding_boundary_against_hand_written_visibility():
+    err, dk, dv = _padding_error(A)
+    assert err <= 1e-12
+    assert np.all(dv[0, 0, 4] != 0.0) and np.all(dk[0, 0, 4] != 0.0)   # key kv_len - 1: visible
+    assert np.all(dv[0, 0, 5:] == 0.0) and np.all(dk[0, 0, 5:] == 0.0)  # key kv_len: hidden
+
+
+def test_padding_pin_catches_an_off_by_one(monkeypatch):
+    _planted(monkeypatch, "padding_off_by_one")
+    assert _padding_error(A)[0] > 1e-2
