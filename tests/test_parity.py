@@ -9,6 +9,7 @@ import torch
 import oracle
 from workloads import WORKLOADS, block_mask_pattern, generate, random_case
 from _gpu_helpers import TOL, f64, max_abs, rel_fro, run, to_device
+from _oracle_pool import key_rows_every_head
 
 pytestmark = pytest.mark.gpu
 
@@ -138,13 +139,11 @@ def test_backward_is_deterministic(fa):
 
 
 # ---------------------------------------------------------------------------
-# long workloads: sampled rows (O, lse, dQ on 256 query rows of every head;
-# dK, dV on 256 key rows of the first KEY_HEADS heads of batch 0, which need
-# the oracle's statistics of every row) plus a property that holds at any size
+# long workloads: sampled rows -- O, lse, dQ on 256 query rows of every head;
+# dK, dV on 256 key rows of every head, which need the oracle's statistics of
+# every query row of the head (computed a head per host core) -- plus
+# properties that hold at any size
 # ---------------------------------------------------------------------------
-
-KEY_HEADS = 2
-
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["long_causal_d128", "block_sparse", "sparse_local_global",
@@ -164,18 +163,17 @@ def test_workload_sampled(fa, name):
     assert max_abs(np.take_along_axis(lse.cpu().numpy().astype(np.float64), rows, axis=2), rl) <= tl
     rdq = oracle.backward_query_rows(case["q"], case["k"], case["v"], case["do"], scale, rows, **kw)
     assert rel_fro(take(f64(dq), rows), rdq) <= tg
-    sl = (slice(0, 1), slice(0, KEY_HEADS))
-    sub = {n: case[n][sl] for n in ("q", "k", "v", "do")}
-    sub_kw = dict(kw)
-    if kw["kv_len"] is not None:
-        sub_kw["kv_len"] = kw["kv_len"][:1]
-    lse_all, d_all = oracle.row_stats(sub["q"], sub["k"], sub["v"], sub["do"], scale, **sub_kw)
-    rdk, rdv = oracle.backward_key_rows(sub["q"], sub["k"], sub["v"], sub["do"], scale,
-                                        cols[sl], lse_all, d_all, **sub_kw)
-    assert rel_fro(take(f64(dk)[sl], cols[sl]), rdk) <= tg
-    assert rel_fro(take(f64(dv)[sl], cols[sl]), rdv) <= tg
-    # the oracle's lse of every row of those heads against the GPU's
-    assert max_abs(lse.cpu().numpy().astype(np.float64)[sl], lse_all) <= tl
+    lse_all, rdk, rdv = key_rows_every_head(case["q"], case["k"], case["v"], case["do"], scale,
+                                            cols, **kw)
+    assert rel_fro(take(f64(dk), cols), rdk) <= tg
+    assert rel_fro(take(f64(dv), cols), rdv) <= tg
+    # per head too, so that one wrong head cannot hide among the others
+    for b in range(w.B):
+        for h in range(w.H):
+            assert rel_fro(take(f64(dk), cols)[b, h], rdk[b, h]) <= tg, ("dK", b, h)
+            assert rel_fro(take(f64(dv), cols)[b, h], rdv[b, h]) <= tg, ("dV", b, h)
+    # the oracle's lse of every row against the GPU's
+    assert max_abs(lse.cpu().numpy().astype(np.float64), lse_all) <= tl
     # any size: shifting every key by one vector leaves O unchanged, so the
     # key gradients of each head sum to zero (bf16 rounding allows a little)
     dk64 = f64(dk)
