@@ -20,10 +20,10 @@ __all__ = [
     "FaError", "FaMask", "FaLayout", "FaLayouts", "FaDropout", "FaBias", "FaOptions", "layout_of",
     "bias_of",
     "make_layouts", "make_options", "fa_fwd_ex", "fa_bwd_ex", "fa_fwd_fp32_ex", "fa_bwd_fp32_ex",
-    "fa_bwd_preprocess_ex", "fa_bwd_dkdv_ex", "fa_bwd_dq_ex", "fa_debug_dropout_mask",
+    "fa_bwd_preprocess_ex", "fa_bwd_dkdv_ex", "fa_bwd_dq_ex",
     "lib", "fa_fwd", "fa_bwd", "fa_bwd_workspace_size",
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_fwd_fp32", "fa_bwd_fp32",
-    "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_umma_gemm", "fa_debug_wait_timeout",
+    "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_wait_timeout",
     "make_mask", "forward", "backward", "LIB_PATH",
     "FA_MASK_NONE", "FA_MASK_KEY_PADDING", "FA_MASK_BLOCK_SPARSE", "STATUS",
 ]
@@ -102,7 +102,6 @@ _SIGS = {
     "fa_bwd_dq": [_p] * 7 + [_i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_status_string": [_i],
     "fa_get_device_status": [_p, ctypes.POINTER(ctypes.c_int)],
-    "fa_debug_umma_gemm": [_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p],
     "fa_debug_wait_timeout": [ctypes.c_uint, _p],
     "fa_bwd_noalloc": [_p] * 9 + [_i, _i, _i, _i, _f, _i, _mp, _p],
     "fa_last_cuda_error": [],
@@ -113,7 +112,6 @@ _SIGS = {
     "fa_bwd_preprocess_ex": [_p, _p, _p, _i, _i, _i, _i, _op, _p],
     "fa_bwd_dkdv_ex": [_p] * 8 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
     "fa_bwd_dq_ex": [_p] * 7 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
-    "fa_debug_dropout_mask": [_p, _i, _i, _i, ctypes.POINTER(FaDropout), _i, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -258,13 +256,6 @@ def fa_bwd_dq_ex(q, k, v, dO, lse, D, dq, B, H, N, d, scale, causal, mask=None, 
            "fa_bwd_dq_ex")
 
 
-def fa_debug_dropout_mask(out, B, H, N, p, seed, offset, path, stream=None):
-    """Writes the keep mask (uint8 [B*H, N, N]) through kernel path 0 (rows) or 1 (keys)."""
-    dr = FaDropout(p, seed, offset)
-    _check(lib.fa_debug_dropout_mask(_ptr(out), B, H, N, ctypes.byref(dr), path,
-                                     _stream(stream)), "fa_debug_dropout_mask")
-
-
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, mask=None, stream=None):
     _check(lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, scale,
                       int(causal), mask, _stream(stream)), "fa_fwd")
@@ -331,12 +322,6 @@ def fa_get_device_status(stream=None):
     site = ctypes.c_int(0)
     code = lib.fa_get_device_status(_stream(stream), ctypes.byref(site))
     return code, site.value
-
-
-def fa_debug_umma_gemm(a, b, d, M, N, K, a_mn_major=0, b_mn_major=0, a_in_tmem=0, use_tma=0,
-                       stream=None):
-    _check(lib.fa_debug_umma_gemm(_ptr(a), _ptr(b), _ptr(d), M, N, K, a_mn_major, b_mn_major,
-                                  a_in_tmem, use_tma, _stream(stream)), "fa_debug_umma_gemm")
 
 
 def fa_debug_wait_timeout(limit_us, stream=None):

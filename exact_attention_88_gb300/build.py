@@ -3,6 +3,11 @@
 Each translation unit is compiled in parallel into `_build/`, then linked into
 `libfa.so` next to this file.  Rebuilds only what changed; objects made on a
 different host architecture are discarded first.
+
+`libfa_diag.so` (from `csrc/diag/`) holds test-only diagnostics -- the
+tensor-core operand-layout GEMM and the dropout-mask writer -- and links
+against libfa.so; it is built beside it for the tests and is not part of
+libfa's C ABI.
 """
 import os
 import platform
@@ -29,6 +34,8 @@ SOURCES = [
     "fa_noalloc.cu",
 ]
 HEADERS = ["fa_common.cuh", "fa_internal.h"]
+DIAG_SOURCES = [os.path.join("diag", "fa_diag.cu")]
+DIAG_LIB = os.path.join(HERE, "libfa_diag.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
@@ -50,7 +57,7 @@ def _newest_dep():
 
 
 def _compile(src, ptxas_verbose=False):
-    obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
     s = os.path.join(CSRC, src)
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(s), _newest_dep()):
         return obj, ""
@@ -61,6 +68,18 @@ def _compile(src, ptxas_verbose=False):
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
     return obj, r.stderr
+
+
+def _link(lib, objs, deps, extra=()):
+    newest = max(os.path.getmtime(p) for p in list(objs) + list(deps))
+    if os.path.exists(lib) and os.path.getmtime(lib) >= newest:
+        return
+    tmp = lib + ".tmp"
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + list(objs) + list(extra)
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
+    os.replace(tmp, lib)
 
 
 def _host_stamp():
@@ -76,24 +95,22 @@ def build(verbose=False, ptxas_verbose=False):
         # objects or a library built on another host architecture: start over
         for f in os.listdir(BUILD):
             os.remove(os.path.join(BUILD, f))
-        if os.path.exists(LIB):
-            os.remove(LIB)
+        for lib in (LIB, DIAG_LIB):
+            if os.path.exists(lib):
+                os.remove(lib)
         with open(stamp, "w") as f:
             f.write(_host_stamp())
-    with ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
-        results = list(ex.map(lambda s: _compile(s, ptxas_verbose), SOURCES))
-    objs = [o for o, _ in results]
+    every = SOURCES + DIAG_SOURCES
+    with ThreadPoolExecutor(max_workers=min(len(every), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(lambda s: _compile(s, ptxas_verbose), every))
+    objs = [o for o, _ in results[:len(SOURCES)]]
+    diag_objs = [o for o, _ in results[len(SOURCES):]]
     if verbose or ptxas_verbose:
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + ".tmp"
-        cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-        os.replace(tmp, LIB)
+    _link(LIB, objs, [])
+    _link(DIAG_LIB, diag_objs, [LIB], extra=["-L", HERE, "-lfa", "-Xlinker", "-rpath=$ORIGIN"])
     return LIB
 
 

@@ -122,6 +122,8 @@ fa_status check_bias(const fa_bias* bias, int N, int esize, const float** ptr, L
   return FA_OK;
 }
 
+}  // namespace
+
 // Validates a dropout request and derives the kernels' parameters: the
 // 16-bit threshold t = min(65535, floor(p 65536 + 1/2)) (keep probability
 // 1 - t/65536 exactly) and the scale 65536 / (65536 - t).  No request, or
@@ -142,8 +144,6 @@ fa_status check_dropout(const fa_dropout* dr, int esize, DropParams* out) {
   out->rp = (float)(65536.0 / (65536.0 - (double)t));
   return FA_OK;
 }
-
-}  // namespace
 
 bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B, int H, int N,
                      int d, int box_rows) {
@@ -270,6 +270,22 @@ static fa_status launched(cudaError_t e) {
   if (e == cudaSuccess) return FA_OK;
   t_last_cuda_error = cudaGetErrorString(e);
   return FA_ERR_CUDA;
+}
+
+fa_status fa::cuda_status(cudaError_t e) { return launched(e); }
+
+fa_status fa::check_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                             const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                             int B, int H, int N, int d, float scale, int causal,
+                             const fa_mask* mask) {
+  BwdArgs a{};
+  fa_status st = fill_bwd_common(&a, B, H, N, d, scale, causal, mask);
+  if (st != FA_OK) return st;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned4(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_ALIGNMENT;
+  return FA_OK;
 }
 
 extern "C" {
@@ -446,33 +462,6 @@ fa_status fa_get_device_status(void* stream, int* site) {
     return h[0] == kStatusTimeoutCode ? FA_ERR_TIMEOUT : FA_ERR_CUDA;
   }
   return FA_OK;
-}
-
-fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int N, int K,
-                             int a_mn_major, int b_mn_major, int a_in_tmem, int use_tma,
-                             void* stream) {
-  if (!a || !b || !d) return FA_ERR_INVALID_ARG;
-  if (M != 128 || (N != 64 && N != 128 && N != 256) || (K != 64 && K != 128))
-    return FA_ERR_UNSUPPORTED;
-  if (a_in_tmem < 0 || a_in_tmem > 3 || (a_in_tmem && a_mn_major)) return FA_ERR_INVALID_ARG;
-  if (use_tma && (a_mn_major || b_mn_major)) return FA_ERR_UNSUPPORTED;
-  if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FA_ERR_ALIGNMENT;
-  int* st = device_status();
-  if (!st) return FA_ERR_CUDA;
-  return launched(launch_umma_probe(a, b, d, M, N, K, a_mn_major, b_mn_major, a_in_tmem, use_tma,
-                                    st, static_cast<cudaStream_t>(stream)));
-}
-
-fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_dropout* dropout,
-                                int path, void* stream) {
-  if (!out || !dropout) return FA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || N < 1 || (long long)B * H > 65535) return FA_ERR_INVALID_ARG;
-  if (N > 4096) return FA_ERR_UNSUPPORTED;
-  if (path != 0 && path != 1) return FA_ERR_INVALID_ARG;
-  DropParams d;
-  const fa_status st = check_dropout(dropout, 2, &d);
-  if (st != FA_OK) return st;
-  return launched(launch_dropout_mask(out, B * H, N, d, path, static_cast<cudaStream_t>(stream)));
 }
 
 fa_status fa_debug_wait_timeout(unsigned int limit_us, void* stream) {

@@ -109,13 +109,21 @@ cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
-cudaError_t launch_umma_probe(const void* a, const void* b, float* d, int M, int N, int K,
-                              int a_mn, int b_mn, int a_tmem, int use_tma, int* status,
-                              cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
-cudaError_t launch_dropout_mask(uint8_t* out, int BH, int N, const DropParams& d, int path,
-                                cudaStream_t s);
-
 inline int tiles_of(int n, int t) { return (n + t - 1) / t; }
+
+// The argument checks of fa_bwd / fa_bwd_ex (bf16), in the same order, short
+// of the workspace: host-only, no CUDA runtime call.
+fa_status check_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                         const void* dO, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int N, int d, float scale, int causal, const fa_mask* mask);
+
+// Validates a dropout request (esize: 2 for bf16, 4 for fp32) and derives the
+// kernels' parameters; no request, or a threshold of 0, is no dropout.
+fa_status check_dropout(const fa_dropout* dr, int esize, DropParams* out);
+
+// Maps a CUDA error to the ABI's status, remembering its text for
+// fa_last_cuda_error() (cudaSuccess: FA_OK).
+fa_status cuda_status(cudaError_t e);
 
 }  // namespace fa

@@ -26,20 +26,23 @@ constexpr int kMaxNoAllocDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 // Device address of the scratch array on the current device, looked up once
-// per device.  Returns nullptr if the lookup fails.
-void* scratch_address() {
+// per device.  On failure returns the CUDA error and leaves *out unset.
+cudaError_t scratch_address(void** out) {
   static void* addr[kMaxNoAllocDevices] = {nullptr};
   static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoAllocDevices) return nullptr;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxNoAllocDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
     addr[dev] = p;
   }
-  return addr[dev];
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -49,13 +52,18 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const void* dO, const float* lse, void* dq, void* dk,
                                     void* dv, int B, int H, int N, int d, float scale, int causal,
                                     const fa_mask* mask, void* stream) {
-  const size_t need = fa_bwd_workspace_size(B, H, N, d);
-  if (need == 0) return (B < 1 || H < 1 || N < 1) ? FA_ERR_INVALID_ARG : FA_ERR_UNSUPPORTED;
-  if (need > fa::kNoAllocScratchBytes) return FA_ERR_UNSUPPORTED;  // beyond the fixed scratch
-  void* scratch = fa::scratch_address();
-  if (!scratch) return FA_ERR_CUDA;
-  // fa_bwd validates every argument and writes D into the scratch before any
-  // kernel reads it, then runs the backward kernels on `stream`.
+  // fa_bwd's own argument checks first, on the host only, so that argument
+  // errors come back with fa_bwd's codes before any CUDA runtime call
+  fa_status st = fa::check_bwd_args(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal,
+                                    mask);
+  if (st != FA_OK) return st;
+  if (fa_bwd_workspace_size(B, H, N, d) > fa::kNoAllocScratchBytes)
+    return FA_ERR_UNSUPPORTED;  // beyond the fixed scratch
+  void* scratch = nullptr;
+  st = fa::cuda_status(fa::scratch_address(&scratch));
+  if (st != FA_OK) return st;
+  // fa_bwd writes D into the scratch before any kernel reads it, then runs
+  // the backward kernels on `stream`.
   return fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, scratch, fa::kNoAllocScratchBytes, B, H, N, d,
                 scale, causal, mask, stream);
 }

@@ -251,7 +251,9 @@ fa_status fa_bwd_dq_ex(const void* q, const void* k, const void* v, const void* 
  * call takes the workspace from a fixed array of FA_NOALLOC_SCRATCH_BYTES
  * compiled into the library (every GPU that loads the library holds it until
  * the process exits) and calls no allocator at all.
- *   Arguments and results are those of fa_bwd without the workspace pair.
+ *   Arguments and results are those of fa_bwd without the workspace pair;
+ *   argument errors come back with fa_bwd's codes, from host-only checks
+ *   made before any CUDA runtime call.
  *   Sizes whose workspace (fa_bwd_workspace_size) exceeds
  *   FA_NOALLOC_SCRATCH_BYTES are rejected with FA_ERR_UNSUPPORTED.
  *   The first call on a device looks up the array's device address (a CUDA
@@ -278,29 +280,6 @@ const char* fa_last_cuda_error(void);
  * FA_ERR_CUDA if the stream reports an error.  FA_OK otherwise.  If site is
  * not NULL it receives the id of the wait that gave up. */
 fa_status fa_get_device_status(void* stream, int* site);
-
-/* Diagnostic: one CTA computes D[M x N] (fp32, row-major) = A B^T on the
- * tensor cores with exactly the operand staging the attention kernels use,
- * so a GPU can be checked for the layouts they rely on.
- *   a : device bf16 [M x K] row-major, b : device bf16 [N x K] row-major,
- *   M = 128, N in {64, 128, 256}, K in {64, 128}.
- *   a_mn_major / b_mn_major : stage the operand M/N-contiguous instead of
- *   K-contiguous.  a_in_tmem : 0 = A from shared memory; 1 = A from tensor
- *   memory, two bf16 per 32-bit column, even k in the low half; 2 = the same
- *   with even k in the high half; 3 = one bf16 per column (1..3 need
- *   a_mn_major = 0).  use_tma : load K-major operands with TMA instead of
- *   plain loads. */
-fa_status fa_debug_umma_gemm(const void* a, const void* b, float* d, int M, int N, int K,
-                             int a_mn_major, int b_mn_major, int a_in_tmem, int use_tma,
-                             void* stream);
-
-/* Diagnostic: writes the dropout keep mask Z (uint8 [B*H, N, N], 1 = kept)
- * of `dropout` with the device code of the attention kernels: path 0 as the
- * forward and dQ kernels draw it (a query row per thread, 32 keep bits at a
- * time), path 1 as the dK/dV kernel does (a key per thread, the bits of each
- * call shared among eight lanes).  `out` is device memory of B*H*N*N bytes; N <= 4096. */
-fa_status fa_debug_dropout_mask(uint8_t* out, int B, int H, int N, const fa_dropout* dropout,
-                                int path, void* stream);
 
 /* Diagnostic: launches one CTA that waits on an mbarrier no one arrives on,
  * with the given limit (1..1000000 microseconds), exactly as the attention

@@ -116,7 +116,7 @@ def bwd(fa, **kw):
     ws = kw.get("ws_bytes", fa.fa_bwd_workspace_size(1, 1, 128, 64))
     return fa.lib.fa_bwd(kw.get("q", FAKE), FAKE, FAKE, FAKE, kw.get("dO", FAKE), FAKE,
                          kw.get("dq", FAKE), FAKE, FAKE, kw.get("ws", FAKE), ws, B, H, N, d,
-                         kw.get("scale", 0.125), 0, None, None)
+                         kw.get("scale", 0.125), kw.get("causal", 0), kw.get("mask"), None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -125,6 +125,35 @@ def bwd(fa, **kw):
 ])
 def test_bwd_rejects_bad_arguments(fa, kw, code):
     assert bwd(fa, **kw) == code
+
+
+def noalloc(fa, **kw):
+    B, H, N, d = kw.get("B", 1), kw.get("H", 1), kw.get("N", 128), kw.get("d", 64)
+    return fa.lib.fa_bwd_noalloc(kw.get("q", FAKE), FAKE, FAKE, FAKE, kw.get("dO", FAKE), FAKE,
+                                 kw.get("dq", FAKE), FAKE, FAKE, B, H, N, d,
+                                 kw.get("scale", 0.125), kw.get("causal", 0), kw.get("mask"),
+                                 None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(dO=0), 1), (dict(dq=FAKE + 4), 3), (dict(d=32), 2), (dict(d=0), 1),
+    (dict(d=-1), 1), (dict(B=0), 1), (dict(scale=-0.1), 1), (dict(causal=3), 1),
+    (dict(B=300, H=300), 2),
+])
+def test_noalloc_rejects_what_fa_bwd_rejects(fa, kw, code):
+    """The allocation-free backward checks its arguments as fa_bwd does, with
+    the same codes, before any CUDA runtime call (no GPU here)."""
+    assert noalloc(fa, **kw) == code
+    assert bwd(fa, **kw) == code
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(fa):
+    # D alone needs 64 MiB for 16 x 16 heads of 65536 rows: more than the
+    # fixed 32 MiB scratch; valid arguments otherwise
+    assert fa.fa_bwd_workspace_size(16, 16, 65536, 128) > fa.NOALLOC_SCRATCH_BYTES
+    assert noalloc(fa, B=16, H=16, N=65536, d=128) == 2
+    m = ctypes.pointer(fa.FaMask(7, None, None, 128))
+    assert noalloc(fa, mask=m) == 1
 
 
 def test_substeps_reject_bad_arguments(fa):
@@ -138,8 +167,6 @@ def test_substeps_reject_bad_arguments(fa):
                             None, None) == 3
     assert fa.lib.fa_bwd_dq(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.1, 2,
                             None, None) == 1
-    assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 64, 128, 64, 0, 0, 0, 0, None) == 2
-    assert fa.lib.fa_debug_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 1, 0, 1, 0, None) == 1
     assert fa.lib.fa_debug_wait_timeout(0, None) == 1
     assert fa.lib.fa_debug_wait_timeout(2000000, None) == 1
 
@@ -228,14 +255,24 @@ def test_dropout_rules(fa, bwd):
                                None, bad, None) == 1
 
 
-def test_dropout_mask_diagnostic_rejects(fa):
+def test_diagnostics_stay_out_of_the_product_abi(fa):
+    """The layout GEMM and the dropout-mask writer live in the test-only
+    libfa_diag.so; libfa.so exports neither, and the test library rejects bad
+    arguments on the host."""
+    out = subprocess.run(["nm", "-D", "--defined-only", fa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    assert "fa_diag_" not in out and "fa_debug_umma" not in out and "dropout_mask" not in out
+    import _diag
+    assert _diag.lib.fa_diag_umma_gemm(FAKE, FAKE, FAKE, 64, 128, 64, 0, 0, 0, 0, None) == 2
+    assert _diag.lib.fa_diag_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 1, 0, 1, 0, None) == 1
+    assert _diag.lib.fa_diag_umma_gemm(FAKE, FAKE, FAKE, 128, 128, 64, 0, 0, 2, 0, None) == 1
     dr = ctypes.byref(fa.FaDropout(0.5, 1, 2))
-    assert fa.lib.fa_debug_dropout_mask(None, 1, 1, 64, dr, 0, None) == 1
-    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, None, 0, None) == 1
-    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 5000, dr, 0, None) == 2
-    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, dr, 2, None) == 1
-    assert fa.lib.fa_debug_dropout_mask(FAKE, 1, 1, 64, ctypes.byref(fa.FaDropout(1.0, 1, 2)), 0,
-                                        None) == 1
+    assert _diag.lib.fa_diag_dropout_mask(None, 1, 1, 64, dr, 0, None) == 1
+    assert _diag.lib.fa_diag_dropout_mask(FAKE, 1, 1, 64, None, 0, None) == 1
+    assert _diag.lib.fa_diag_dropout_mask(FAKE, 1, 1, 5000, dr, 0, None) == 2
+    assert _diag.lib.fa_diag_dropout_mask(FAKE, 1, 1, 64, dr, 2, None) == 1
+    assert _diag.lib.fa_diag_dropout_mask(FAKE, 1, 1, 64, ctypes.byref(fa.FaDropout(1.0, 1, 2)),
+                                          0, None) == 1
 
 
 def test_bias_rules(fa):
