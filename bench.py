@@ -39,7 +39,13 @@ DEFAULT_WORKLOAD = "long_causal_d128"
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # current version of that kernel; set to None whenever the kernel changes
 # until it is captured again.
-DKDV_DRAM_BYTES = {"long_causal_d128": 380852480 + 103521280}
+DKDV_DRAM_BYTES = {"long_causal_d128": 374785536 + 103186432}
+# Tensor-pipe activity of each kernel on the default workload: the fraction of
+# elapsed cycles the tensor pipe was active (sm__pipe_tensor_cycles_active,
+# pct_of_peak_sustained_elapsed) in one-kernel ncu captures of the current
+# kernels; set to None whenever a kernel changes until it is captured again.
+TENSOR_PIPE_ACTIVE = {"long_causal_d128": {"fwd": 0.506, "bwd_preprocess": 0.0,
+                                           "bwd_dkdv": 0.603, "bwd_dq": 0.698}}
 
 
 def measured_peaks():
@@ -437,6 +443,8 @@ def run_gpu(args, rank, world, local_rank):
                         "achieved": round(dq_achieved, 2), "frac": round(dq_achieved / peak, 4),
                         "flops_per_launch": dq_flops},
         "gpu_launches": 4 * args.steps,
+        "tensor_pipe": tensor_pipe_share(w.name, per_kernel, step_flops, fwd_flops),
+        "peak_clocks": peak_clock_note(peaks, clocks),
         "clocks": clocks,
         "device": device_info(dev, sampler.driver),
     }
@@ -451,6 +459,37 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_extras:
         result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt)
     return result
+
+
+def tensor_pipe_share(workload, per_kernel_ms, step_flops, fwd_flops):
+    """The step's tensor-pipe activity from the ncu captures of each kernel,
+    weighted by this run's kernel times, and the share of it that is
+    algorithmic work: the kernels execute fwd (2 GEMMs), dK/dV (4) and dQ (3,
+    of which S and dP are a second recomputation) = 4.5 x fwd_flops, while the
+    metric counts 3.5 x fwd_flops."""
+    act = TENSOR_PIPE_ACTIVE.get(workload)
+    if not act or any(v is None for v in act.values()):
+        return None
+    total = sum(per_kernel_ms.values())
+    busy = sum(act[k] * per_kernel_ms[k] for k in act) / total
+    executed = fwd_flops + 2.0 * fwd_flops + 1.5 * fwd_flops
+    return {"active_time_weighted": round(busy, 4),
+            "executed_tflop": round(executed / 1e12, 4),
+            "algorithmic_tflop": round(step_flops / 1e12, 4),
+            "algorithmic_active": round(busy * step_flops / executed, 4),
+            "per_kernel_active": act,
+            "source": "one-kernel ncu --set full captures (sm__pipe_tensor_cycles_active, "
+                      "% of elapsed cycles), weighted by this run's per-kernel times"}
+
+
+def peak_clock_note(peaks, clocks):
+    """The SM clock the measured GEMM peak was taken at beside this run's."""
+    under = peaks.get("clocks_under_load") or {}
+    return {"peak_gemm_sm_mhz_median": under.get("sm_mhz_median"),
+            "this_run_sm_mhz_median": (clocks or {}).get("sm_mhz"),
+            "note": "the measured bf16 peak comes from cuBLAS GEMMs whose SM clock under the "
+                    "power cap had the median above; the attention kernels run at the clock "
+                    "of this run"}
 
 
 def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None):
@@ -590,6 +629,81 @@ def cpu_baseline(w, case, n_rows, heads):
                       % (n_rows, n_slices, w.name, w.N, sec)}
 
 
+def cpu_model():
+    """The host CPU's model name (x86: /proc/cpuinfo "model name"; Arm: lscpu's
+    "Model name", which names the core, e.g. Neoverse-V2)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+# the five workloads the metric's configurations name, in their order
+ORACLE_TIME_WORKLOADS = ["tiny_fp32", "tiny_fp32_causal", "gpt2_causal", "bert_padding",
+                         "long_causal_d128", "block_sparse"]
+
+
+def oracle_times(rows_per_block=2048):
+    """Host time of the fp64 oracle on every configuration: the whole forward +
+    backward where it fits (the short workloads), else one whole (batch, head)
+    slice -- every query row, in blocks of rows, forward and backward -- scaled
+    by B*H and labelled "extrapolated", plus the wall time of the sampled-row
+    check the parity tests make (O, lse, dQ of 256 query rows per head).  One
+    JSON line per workload."""
+    import oracle
+    out = []
+    for name in ORACLE_TIME_WORKLOADS:
+        w = WORKLOADS[name]
+        case = generate(w, seed=0, samples=256)
+        kept = kept_fraction(case["block_mask"])
+        fwd_fl, step_fl = flops(w, kept)
+        kw = dict(causal=w.causal, kv_len=case["kv_len"], block_mask=case["block_mask"])
+        rec = {"workload": name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+               "mask": w.mask, "cores": host_cores(), "cpu": cpu_model(),
+               "algorithmic_gflop_fwd_bwd": round(step_fl / 1e9, 3)}
+        if not w.sampled:
+            t0 = time.perf_counter()
+            oracle.forward(case["q"], case["k"], case["v"], w.scale, **kw)
+            oracle.backward(case["q"], case["k"], case["v"], case["do"], w.scale, **kw)
+            sec = time.perf_counter() - t0
+            rec.update(kind="whole workload, forward + backward", seconds=round(sec, 3),
+                       tflops=round(step_fl / sec / 1e12, 6))
+        else:
+            t0 = time.perf_counter()
+            for r0 in range(0, w.N, rows_per_block):
+                oracle.row_block_forward_backward(case["q"], case["k"], case["v"], case["do"],
+                                                  w.scale, 0, 0,
+                                                  np.arange(r0, min(w.N, r0 + rows_per_block)),
+                                                  **kw)
+            sec = time.perf_counter() - t0
+            slices = w.B * w.H
+            rec.update(kind="one (batch, head) slice, forward + backward of every row, x B*H: "
+                            "extrapolated",
+                       seconds_one_slice=round(sec, 3),
+                       seconds=round(sec * slices, 1),
+                       tflops=round(step_fl / (sec * slices) / 1e12, 6))
+            t0 = time.perf_counter()
+            oracle.forward_rows(case["q"], case["k"], case["v"], w.scale, case["rows"], **kw)
+            oracle.backward_query_rows(case["q"], case["k"], case["v"], case["do"], w.scale,
+                                       case["rows"], **kw)
+            rec["sampled_query_rows_check_seconds"] = round(time.perf_counter() - t0, 3)
+        out.append(rec)
+        print(json.dumps(rec), flush=True)
+    return out
+
+
 def run_reference(args, rank):
     if rank != 0:
         return None
@@ -634,7 +748,14 @@ def main():
                     help="(batch, head) slices in the CPU baseline's sample (about 2 s each "
                          "on the long causal workload)")
     ap.add_argument("--reference-rows", type=int, default=2048)
+    ap.add_argument("--oracle-times", action="store_true",
+                    help="time the fp64 oracle on the host for every configuration (no GPU) "
+                         "and print one JSON line per workload")
     args = ap.parse_args()
+
+    if args.oracle_times:
+        oracle_times()
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
