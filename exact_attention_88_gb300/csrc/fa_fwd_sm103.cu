@@ -8,30 +8,33 @@
 // Online Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)").  The
 // division by l is deferred to the end, which is the same quantity.
 //
-// One CTA owns two 128-row query tiles (A and B) of one (batch, head) and
-// streams the key/value tiles through a shared ring.  The two tiles alternate
-// on the tensor core: while one tile's softmax runs on its warpgroup, the other
-// tile's S = Q K^T or O += P V is computed, so the tensor core has work
-// queued.  TMEM columns: S_A / P_A [0,128), O_A [128, 128+d), S_B / P_B
-// [256, 384), O_B [384, 384+d).
+// d = 128: one CTA owns two 128-row query tiles (A and B) of one (batch,
+// head) and streams the key/value tiles through a shared ring.  The two tiles
+// alternate on the tensor core: while one tile's softmax runs on its
+// warpgroup, the other tile's S = Q K^T or O += P V is computed, so the tensor
+// core has work queued.  TMEM columns: S_A / P_A [0,128), O_A [128, 128+d),
+// S_B / P_B [256, 384), O_B [384, 384+d).
+// d = 64: one CTA owns one query tile (S / P [0, 128), O [128, 192) of 256
+// TMEM columns, 81 KB of shared memory), and two CTAs share an SM: one's
+// set-up, first loads and epilogue run under the other's work, and a CTA walks
+// only the key tiles its own tile sees.
 //
-// Roles (352 threads):
-//   warps 0-3, 4-7  softmax of tile A, B: thread t owns row t (TMEM lane t);
-//                   at d = 128 the two take turns key tile by key tile, at
-//                   d = 64 they run side by side;
+// Roles (d = 128: 352 threads; d = 64: 192):
+//   warps 0-3 (, 4-7) softmax of tile A (, B): thread t owns row t (TMEM lane
+//                   t); at d = 128 the two take turns key tile by key tile;
 //                   reads its 128 scores (max, then exponentials), masks,
 //                   updates m and l, writes P~ = 2^(c S - m) as packed bf16
 //                   over the S columns,
 //                   rescales O in TMEM when m grew by more than 8 in log2 units
 //                   (lazy rescale), and at the end writes O / l and lse.
-//   warp 8          TMA producer: Q_A, Q_B once, then K_j / V_j into rings.
-//   warps 9, 10     MMA issuers for tile A, B (one thread each).
+//   warp 8 (4)      TMA producer: the Q tiles once, then K_j / V_j into rings.
+//   warps 9, 10 (5) MMA issuers for tile A, B (one thread each).
 // Scores are kept in base 2: c = scale * log2(e); lse = ln2 * (m + log2 l).
 //
 // Every tensor is read through a 4-D TMA descriptor (column, row, head, batch)
 // carrying its own strides, and O is stored through its strides, so any layout
-// with contiguous rows costs nothing.  A block-sparse CTA copies its two rows
-// of the tile mask into shared-memory bitmaps first.  The kExtra variant adds
+// with contiguous rows costs nothing.  A block-sparse CTA copies its rows of
+// the tile mask into shared-memory bitmaps first.  The kExtra variant adds
 // dropout (a row's 128 keep bits of a tile are drawn before its turn; dropped
 // entries of P~ are zeroed after l has summed them; O is scaled by 1/(1-p) at
 // the end) and an additive bias (added to the scaled scores in the max pass,
@@ -46,24 +49,28 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P~ stays below 2^8
 
-template <int D>
+template <int D, int kTiles>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;             // 64-column (128-byte) chunks
   static constexpr int kTileBytes = 128 * D * 2;     // one Q, K or V tile
   static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 128 bytes
-  static constexpr int kStages = (D == 64) ? 3 : 2;  // K/V ring depth
-  static constexpr int kOffQ = 0;                    // Q_A, Q_B
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  // K/V ring depth; a one-tile CTA keeps two stages so that two CTAs fit an SM
+  static constexpr int kStages = kTiles == 1 ? 2 : (D == 64) ? 3 : 2;
+  static constexpr int kOffQ = 0;                    // Q_A (, Q_B)
+  static constexpr int kOffK = kOffQ + kTiles * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kSmem = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
-  static constexpr int kTmemCols = 512;
-  static constexpr int kThreads = 352;
-  // d = 128: the two softmax warpgroups take turns key tile by key tile, so
-  // that each runs alone while the tensor core works for the other tile (run
-  // side by side, the two tiles' MMAs bunch up and the pipe idles while both
-  // passes run).  d = 64: the MMAs are half as long and the passes, bound by
-  // the MUFU, set the pace; run side by side they share it better (block-sparse
-  // forward 0.664 against 0.734 ms measured).
+  static constexpr int kTmemCols = kTiles == 2 ? 512 : 256;          // (S, O) per tile
+  static constexpr int kSoftmaxWarps = 4 * kTiles;
+  static constexpr int kProducerWarp = kSoftmaxWarps;
+  static constexpr int kIssuerWarp0 = kSoftmaxWarps + 1;             // one issuer per tile
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 1 + kTiles);
+  static constexpr int kMinBlocks = kTiles == 2 ? 1 : 2;             // CTAs per SM
+  // d = 128 (two tiles): the two softmax warpgroups take turns key tile by key
+  // tile, so that each runs alone while the tensor core works for the other
+  // tile (run side by side, the two tiles' MMAs bunch up and the pipe idles
+  // while both passes run).  d = 64 keeps one query tile per CTA and two CTAs
+  // per SM, whose softmax passes run side by side.
   static constexpr bool kTurns = D == 128;
 };
 
@@ -235,11 +242,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t tS, uint32_t tO, int ocols
   tmem_wait_st();
 }
 
-template <int D, bool kExtra>
-__global__ void __launch_bounds__(352, 1)
+template <int D, bool kExtra, int kTiles>
+__global__ void __launch_bounds__(FwdCfg<D, kTiles>::kThreads, FwdCfg<D, kTiles>::kMinBlocks)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kTiles>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -261,8 +268,9 @@ __global__ void __launch_bounds__(352, 1)
   const int pair = p.pairs - 1 - order;
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
-  const int qa = 2 * pair, qb = 2 * pair + 1;  // query tiles; qb may be past the end
-  const bool has_b = qb < p.T;
+  // query tiles (p.pairs counts the CTAs' units: pairs of tiles, or tiles)
+  const int qa = kTiles == 2 ? 2 * pair : pair, qb = 2 * pair + 1;  // qb may be past the end
+  const bool has_b = kTiles == 2 && qb < p.T;
 
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
@@ -291,19 +299,19 @@ __global__ void __launch_bounds__(352, 1)
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 2);  // one commit from each issuer
-      mbar_init(&v_empty[s], 2);
+      mbar_init(&k_empty[s], kTiles);  // one commit from each issuer
+      mbar_init(&v_empty[s], kTiles);
     }
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) tmem_alloc(&tmem_slot, C::kTmemCols);
+  if (warp == C::kIssuerWarp0) tmem_alloc(&tmem_slot, C::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
-  if (warp == 8) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tmQ);
@@ -344,7 +352,7 @@ __global__ void __launch_bounds__(352, 1)
         if (vcount[s]) mbar_drain(&v_full[s], (vcount[s] - 1) & 1);
       }
     }
-  } else if (warp == 9 || warp == 10) {
+  } else if (warp >= C::kIssuerWarp0) {
     // ------------------------------------------------------------ MMA issuers
     // One issuing thread per query tile (warp 9: A, warp 10: B): an MMA costs
     // its issuing thread about as long as the tensor core takes to run it, so
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(352, 1)
     // tile's MMAs.  Both walk the key tiles either tile sees and release each
     // K / V stage with a commit of their own (the stage barriers count two).
     // (B runs even without a tile B: it still owes its commit for every stage)
-    const int x = warp - 9;
+    const int x = warp - C::kIssuerWarp0;
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(128, 128, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(128, D, false, true);
@@ -507,15 +515,15 @@ __global__ void __launch_bounds__(352, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) {
+  if (warp == C::kIssuerWarp0) {
     __syncwarp();
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
-template <int D>
+template <int D, int kTiles>
 cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kTiles>;
   const int BH = a.B * a.H;
   CUtensorMap mq, mk, mv;
   if (!encode_bhnd_map(&mq, a.q, a.lq, a.B, a.H, a.N, D, 128) ||
@@ -531,7 +539,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.H = a.H;
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
-  p.pairs = (p.T + 1) / 2;
+  p.pairs = kTiles == 2 ? (p.T + 1) / 2 : p.T;
   p.BH = BH;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
@@ -539,7 +547,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.drop = a.drop;
   p.bias = a.bias;
   p.lb = a.lb;
-  auto kernel = (a.drop.t || a.bias) ? fa_fwd_kernel<D, true> : fa_fwd_kernel<D, false>;
+  auto kernel = (a.drop.t || a.bias) ? fa_fwd_kernel<D, true, kTiles> : fa_fwd_kernel<D, false, kTiles>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.pairs * BH);
@@ -550,7 +558,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
-  return a.d == 64 ? launch_fwd_d<64>(a, s) : launch_fwd_d<128>(a, s);
+  return a.d == 64 ? launch_fwd_d<64, 1>(a, s) : launch_fwd_d<128, 2>(a, s);
 }
 
 }  // namespace fa
