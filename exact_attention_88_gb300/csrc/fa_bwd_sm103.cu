@@ -602,6 +602,8 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s) {
+  // d = 64 calls without dropout or a bias: 64-row steps, two CTAs per SM
+  if (a.d == 64 && !a.drop.t && !a.bias) return launch_bwd_dkdv64_bf16(a, s);
   return a.d == 64 ? launch_dkdv_d<64>(a, s) : launch_dkdv_d<128>(a, s);
 }
 
