@@ -28,6 +28,7 @@ SOURCES = [
     "fa_fwd_sm103.cu",
     "fa_bwd_sm103.cu",
     "fa_bwd_dkdv64_sm103.cu",
+    "fa_bwd_dq64_sm103.cu",
     "fa_bwd_dq_sm103.cu",
     "fa_bwd_aux.cu",
     "fa_fp32.cu",

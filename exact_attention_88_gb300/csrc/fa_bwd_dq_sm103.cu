@@ -455,6 +455,7 @@ cudaError_t launch_dq_d(const BwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s) {
+  if (a.d == 64 && !a.drop.t && !a.bias) return launch_bwd_dq64_bf16(a, s);
   return a.d == 64 ? launch_dq_d<64>(a, s) : launch_dq_d<128>(a, s);
 }
 

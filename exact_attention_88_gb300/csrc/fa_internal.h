@@ -108,6 +108,7 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
 cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_dq64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
 cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
