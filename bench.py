@@ -283,7 +283,13 @@ def run_gpu(args, rank, world, local_rank):
     scale = w.scale
     kv_len = None if case["kv_len"] is None else torch.from_numpy(case["kv_len"]).to(dev)
     bmask = None if case["block_mask"] is None else torch.from_numpy(case["block_mask"]).to(dev)
-    mask = fa.make_mask(kv_len, bmask)
+    # block-sparse: the mask's work order (query tiles, key tiles, pairs, most
+    # work first), recomputed inside every timed step
+    order = None
+    if bmask is not None:
+        order = torch.empty(fa.fa_block_mask_order_len(bmask.shape[0]), dtype=torch.int32,
+                            device=dev)
+    mask = fa.make_mask(kv_len, bmask, tile_order=order)
     # fused dropout (--dropout p): the same kernels with the mask drawn in them
     opt = fa.make_options(None, args.dropout, 0x5EED, 1) if args.dropout else None
     kept = kept_fraction(case["block_mask"])
@@ -310,7 +316,8 @@ def run_gpu(args, rank, world, local_rank):
     D = ws[: rows * 4].view(torch.float32)
     stream = torch.cuda.current_stream(dev)
 
-    kernels = ["fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
+    kernels = (["mask_order"] if order is not None else []) + [
+        "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
     ev = {n: [] for n in kernels}
     # dK/dV and dQ read the same inputs and write disjoint outputs: in the timed
     # steps dQ runs on a second stream, so either kernel's last CTAs overlap
@@ -328,6 +335,9 @@ def run_gpu(args, rank, world, local_rank):
                 ev[name].append((a, b))
             else:
                 fn()
+        if order is not None:
+            mark("mask_order", lambda: fa.fa_block_mask_order(bmask, bmask.shape[0], w.causal,
+                                                              order, stream))
         mark("fwd", lambda: fa.fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, opt,
                                          stream))
         mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
@@ -442,7 +452,8 @@ def run_gpu(args, rank, world, local_rank):
         "dq_roofline": {"kernel": "fa_bwd_dq (S, dP, dQ on tcgen05; S and dP recomputed)",
                         "achieved": round(dq_achieved, 2), "frac": round(dq_achieved / peak, 4),
                         "flops_per_launch": dq_flops},
-        "gpu_launches": 4 * args.steps,
+        # fwd, preprocess, dK/dV, dQ (+ the two work-order kernels when block-sparse)
+        "gpu_launches": (4 + (2 if order is not None else 0)) * args.steps,
         "tensor_pipe": tensor_pipe_share(w.name, per_kernel, step_flops, fwd_flops),
         "peak_clocks": peak_clock_note(peaks, clocks),
         "clocks": clocks,
@@ -457,7 +468,8 @@ def run_gpu(args, rank, world, local_rank):
             "value": round(world * eff_step_flops * args.steps / (elapsed_ms * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "note": "sum_b N * kv_len[b] in place of B * N^2"}
     if not args.no_extras:
-        result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt)
+        result["e2e"] = run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt,
+                                bmask, order)
     return result
 
 
@@ -492,7 +504,8 @@ def peak_clock_note(peaks, clocks):
                     "of this run"}
 
 
-def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None):
+def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None, bmask=None,
+            order=None):
     """Same metric through the public API with host buffers: every step copies
     its inputs in from pinned host memory, runs fa_fwd and the three backward
     steps (dQ on a second stream, as in the device-resident steps) and copies
@@ -538,6 +551,8 @@ def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None):
         s_comp.wait_event(in_ready[k % 2])
         if k >= 2:
             s_comp.wait_event(out_done[k % 2])  # step k-2's results have left this set
+        if order is not None:
+            fa.fa_block_mask_order(bmask, bmask.shape[0], w.causal, order, s_comp)
         fa.fa_fwd_ex(x["q"], x["k"], x["v"], y["o"], y["lse"], B, H, N, d, w.scale, w.causal, mask,
                      opt, s_comp)
         fa.fa_bwd_preprocess(y["o"], x["do"], D, B, H, N, d, s_comp)

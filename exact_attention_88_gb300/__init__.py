@@ -25,6 +25,7 @@ __all__ = [
     "fa_bwd_preprocess", "fa_bwd_dkdv", "fa_bwd_dq", "fa_fwd_fp32", "fa_bwd_fp32",
     "fa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "fa_status_string", "fa_get_device_status", "fa_debug_wait_timeout",
     "make_mask", "forward", "backward", "LIB_PATH",
+    "fa_block_mask_order", "fa_block_mask_order_len", "block_mask_order",
     "FA_MASK_NONE", "FA_MASK_KEY_PADDING", "FA_MASK_BLOCK_SPARSE", "STATUS",
 ]
 
@@ -46,7 +47,8 @@ class FaError(RuntimeError):
 
 class FaMask(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("kv_len", ctypes.c_void_p),
-                ("block_mask", ctypes.c_void_p), ("block_size", ctypes.c_int)]
+                ("block_mask", ctypes.c_void_p), ("block_size", ctypes.c_int),
+                ("tile_order", ctypes.c_void_p)]
 
 
 class FaLayout(ctypes.Structure):
@@ -112,6 +114,8 @@ _SIGS = {
     "fa_bwd_preprocess_ex": [_p, _p, _p, _i, _i, _i, _i, _op, _p],
     "fa_bwd_dkdv_ex": [_p] * 8 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
     "fa_bwd_dq_ex": [_p] * 7 + [_i, _i, _i, _i, _f, _i, _mp, _op, _p],
+    "fa_block_mask_order_len": [_i],
+    "fa_block_mask_order": [_p, _i, _i, _p, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -144,15 +148,19 @@ def _check(code, where):
         raise FaError(code, where, detail)
 
 
-def make_mask(kv_len=None, block_mask=None, block_size=128):
+def make_mask(kv_len=None, block_mask=None, block_size=128, tile_order=None):
     """A pointer to an fa_mask for key padding (kv_len) or a block-sparse tile
-    mask (device tensors), or None for no mask."""
+    mask (device tensors), or None for no mask.  tile_order: the block mask's
+    work order (block_mask_order), or None for the default order."""
     if kv_len is not None and block_mask is not None:
         raise ValueError("one mask kind at a time")
+    if tile_order is not None and block_mask is None:
+        raise ValueError("tile_order belongs to a block mask")
     if kv_len is not None:
-        return ctypes.pointer(FaMask(FA_MASK_KEY_PADDING, _ptr(kv_len), None, block_size))
+        return ctypes.pointer(FaMask(FA_MASK_KEY_PADDING, _ptr(kv_len), None, block_size, None))
     if block_mask is not None:
-        return ctypes.pointer(FaMask(FA_MASK_BLOCK_SPARSE, None, _ptr(block_mask), block_size))
+        return ctypes.pointer(FaMask(FA_MASK_BLOCK_SPARSE, None, _ptr(block_mask), block_size,
+                                     _ptr(tile_order)))
     return None
 
 
@@ -313,6 +321,28 @@ def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, m
                               _stream(stream)), "fa_bwd_noalloc")
 
 
+def fa_block_mask_order_len(T):
+    return lib.fa_block_mask_order_len(T)
+
+
+def fa_block_mask_order(block_mask, T, causal, tile_order, stream=None):
+    _check(lib.fa_block_mask_order(_ptr(block_mask), T, int(causal), _ptr(tile_order),
+                                   _stream(stream)), "fa_block_mask_order")
+
+
+def block_mask_order(block_mask, causal=False, stream=None):
+    """The work order of a [T, T] uint8 CUDA block mask (an int32 CUDA
+    tensor of fa_block_mask_order_len(T) entries), for make_mask(tile_order=)."""
+    import torch
+    T = int(block_mask.shape[0])
+    n = fa_block_mask_order_len(T)
+    if n == 0 or block_mask.numel() != T * T:
+        raise ValueError("expected a [T, T] block mask with 1 <= T <= 4096")
+    out = torch.empty(n, dtype=torch.int32, device=block_mask.device)
+    fa_block_mask_order(block_mask, T, causal, out, stream)
+    return out
+
+
 def fa_status_string(code):
     return lib.fa_status_string(code).decode()
 
@@ -342,19 +372,20 @@ def _shape(q, *others):
 
 
 def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, stream=None,
-            dropout_p=0.0, seed=0, offset=0, bias=None):
+            dropout_p=0.0, seed=0, offset=0, bias=None, tile_order=None):
     """(O, lse) for CUDA tensors q, k, v [B,H,N,d] (bf16 or fp32) of any layout
     whose last dimension is contiguous; O takes q's layout where torch can
     keep it (torch.empty_like).  dropout_p > 0 drops attention probabilities
     (bf16 only); the backward needs the same dropout_p, seed and offset.
     bias: fp32 tensor broadcastable to [B, H, N, N] added to the scaled
-    scores (bf16 only); the backward needs it too."""
+    scores (bf16 only); the backward needs it too.  tile_order: the block
+    mask's work order (block_mask_order), optional."""
     import torch
     B, H, N, d = _shape(q, k, v)
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    mask = make_mask(kv_len, block_mask)
+    mask = make_mask(kv_len, block_mask, tile_order=tile_order)
     opt = make_options(make_layouts(q=q, k=k, v=v, o=o), dropout_p, seed, offset,
                        None if bias is None else bias_of(bias))
     fn = fa_fwd_ex if q.dtype == torch.bfloat16 else fa_fwd_fp32_ex
@@ -363,7 +394,8 @@ def forward(q, k, v, scale=None, causal=False, kv_len=None, block_mask=None, str
 
 
 def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_mask=None,
-             stream=None, workspace=None, dropout_p=0.0, seed=0, offset=0, bias=None):
+             stream=None, workspace=None, dropout_p=0.0, seed=0, offset=0, bias=None,
+             tile_order=None):
     """(dQ, dK, dV) for the forward above and output gradient do; each
     gradient takes the layout of its input where torch can keep it."""
     import torch
@@ -373,7 +405,7 @@ def backward(q, k, v, o, do, lse, scale=None, causal=False, kv_len=None, block_m
     ws_bytes = fa_bwd_workspace_size(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    mask = make_mask(kv_len, block_mask)
+    mask = make_mask(kv_len, block_mask, tile_order=tile_order)
     layouts = make_layouts(q=q, k=k, v=v, o=o, dO=do, dq=dq, dk=dk, dv=dv)
     opt = make_options(layouts, dropout_p, seed, offset, None if bias is None else bias_of(bias))
     fn = fa_bwd_ex if q.dtype == torch.bfloat16 else fa_bwd_fp32_ex

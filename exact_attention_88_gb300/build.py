@@ -34,6 +34,7 @@ SOURCES = [
     "fa_fp32.cu",
     "fa_probe.cu",
     "fa_noalloc.cu",
+    "fa_tile_order.cu",
 ]
 HEADERS = ["fa_common.cuh", "fa_internal.h"]
 DIAG_SOURCES = [os.path.join("diag", "fa_diag.cu")]

@@ -48,12 +48,14 @@ fa_status check_sizes(int B, int H, int N, int d) {
 
 // Tiles of one block-mask row the kernels can hold as a shared-memory bitmap.
 constexpr int kMaxMaskTiles = 4096;
+static_assert(kMaxMaskTiles == kMaxTileOrder, "one limit on the block-mask side");
 
 fa_status check_mask(const fa_mask* m, int N, int* kind, const int32_t** kv,
-                     const uint8_t** bm) {
+                     const uint8_t** bm, const int32_t** order) {
   *kind = FA_MASK_NONE;
   *kv = nullptr;
   *bm = nullptr;
+  *order = nullptr;
   if (!m) return FA_OK;
   switch (m->kind) {
     case FA_MASK_NONE:
@@ -67,8 +69,10 @@ fa_status check_mask(const fa_mask* m, int N, int* kind, const int32_t** kv,
       if (!m->block_mask) return FA_ERR_INVALID_ARG;
       if (m->block_size != 128) return FA_ERR_UNSUPPORTED;
       if (tiles_of(N, 128) > kMaxMaskTiles) return FA_ERR_UNSUPPORTED;
+      if (m->tile_order && !aligned4(m->tile_order)) return FA_ERR_ALIGNMENT;
       *kind = FA_MASK_BLOCK_SPARSE;
       *bm = m->block_mask;
+      *order = m->tile_order;
       return FA_OK;
     default:
       return FA_ERR_INVALID_ARG;
@@ -203,7 +207,7 @@ static fa_status fill_fwd(FwdArgs* a, const void* q, const void* k, const void* 
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned4(lse))
     return FA_ERR_ALIGNMENT;
-  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask);
+  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask, &a->tile_order);
   if (st != FA_OK) return st;
   a->q = q; a->k = k; a->v = v; a->o = o; a->lse = lse;
   a->B = B; a->H = H; a->N = N; a->d = d;
@@ -228,7 +232,7 @@ static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float s
     if ((st = check_layout(in[t], B, H, N, d, esize, out[t])) != FA_OK) return st;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!scale_ok(scale)) return FA_ERR_INVALID_ARG;
-  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask);
+  st = check_mask(mask, N, &a->mask_kind, &a->kv_len, &a->block_mask, &a->tile_order);
   if (st != FA_OK) return st;
   a->B = B; a->H = H; a->N = N; a->d = d;
   a->scale = scale;
@@ -444,6 +448,17 @@ fa_status fa_bwd_fp32_ex(const float* q, const float* k, const float* v, const f
                                H, N, d, scale, causal, mask, options, 4);
   if (st != FA_OK) return st;
   return launched(launch_bwd_fp32(a, static_cast<cudaStream_t>(stream)));
+}
+
+int fa_block_mask_order_len(int T) { return tile_order_len(T); }
+
+fa_status fa_block_mask_order(const uint8_t* block_mask, int T, int causal, int32_t* tile_order,
+                              void* stream) {
+  if (!block_mask || !tile_order || tile_order_len(T) == 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!aligned4(tile_order)) return FA_ERR_ALIGNMENT;
+  return launched(
+      launch_tile_order(block_mask, T, causal, tile_order, static_cast<cudaStream_t>(stream)));
 }
 
 const char* fa_last_cuda_error(void) { return t_last_cuda_error; }

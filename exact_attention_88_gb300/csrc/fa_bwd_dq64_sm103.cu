@@ -64,6 +64,7 @@ struct Dq64Params {
   Layout ldq;
   const int32_t* kv_len;
   const uint8_t* block_mask;
+  const int32_t* order;  // block-sparse work order (query tiles) or nullptr
   int H, N, T, BH;
   float scale, scale_log2;
   int causal;
@@ -105,7 +106,9 @@ __global__ void __launch_bounds__(Dq64Cfg::kThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int order, bh;
   grid_order(blockIdx.x, p.BH, p.T, &order, &bh);
-  const int qi = p.T - 1 - order;  // causal: the last query tiles see the most keys: first
+  // causal: the last query tiles see the most keys: first; a block-sparse
+  // work order lists the query tiles by their visible key tiles
+  const int qi = ordered_tile(p.order, order, p.T, p.T - 1 - order);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   int kv_limit = p.N;
@@ -399,6 +402,7 @@ cudaError_t launch_bwd_dq64_bf16(const BwdArgs& a, cudaStream_t s) {
   p.H = a.H;
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
+  p.order = p.block_mask ? a.tile_order : nullptr;  // query tiles at [0, T)
   p.BH = BH;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;

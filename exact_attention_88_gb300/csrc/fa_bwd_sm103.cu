@@ -78,6 +78,7 @@ struct BwdParams {
   Layout lb;
   const int32_t* kv_len;
   const uint8_t* block_mask;
+  const int32_t* order;  // block-sparse work order (key tiles) or nullptr
   int H, N, T, BH;
   float scale, scale_log2;
   int causal;
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int kt, bh;  // key tile (causal: low tiles have the most work: first)
   grid_order(blockIdx.x, p.BH, p.T, &kt, &bh);
+  kt = ordered_tile(p.order, kt, p.T, kt);  // block-sparse work order: by query tiles seen
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   int kv_limit = p.N;
@@ -586,6 +588,7 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   p.H = a.H;
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
+  p.order = p.block_mask && a.tile_order ? a.tile_order + p.T : nullptr;  // key tiles at [T, 2T)
   p.BH = BH;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;

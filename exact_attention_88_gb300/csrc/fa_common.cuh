@@ -297,6 +297,12 @@ __device__ __forceinline__ void load_bias_row(const float* brow, int k0, int n_k
 // ---------------------------------------------------------------------------
 constexpr int kGroupHeads = 8;
 
+// Tile taken by order index t: entry t of a block-sparse work order when the
+// caller gives one (clamped to [0, n)), else `fallback`.
+__device__ __forceinline__ int ordered_tile(const int32_t* order, int t, int n, int fallback) {
+  return order ? min(max(__ldg(order + t), 0), n - 1) : fallback;
+}
+
 __device__ __forceinline__ void grid_order(int lin, int BH, int nt, int* t, int* bh) {
   const int per_group = kGroupHeads * nt;
   const int g = lin / per_group;

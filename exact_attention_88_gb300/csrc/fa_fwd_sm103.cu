@@ -83,6 +83,7 @@ struct FwdParams {
   float* lse;
   const int32_t* kv_len;
   const uint8_t* block_mask;
+  const int32_t* order;  // block-sparse work order of the units (pairs or tiles), or nullptr
   int H, N, T, BH, pairs;
   float scale_log2;
   int causal;
@@ -262,10 +263,11 @@ __global__ void __launch_bounds__(FwdCfg<D, kTiles>::kThreads, FwdCfg<D, kTiles>
   __shared__ uint32_t mask_bits[2][kMaskBitmapWords];  // block-mask rows qa, qb
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // heaviest pairs first (causal rows near the end see the most keys)
+  // heaviest pairs first: causal rows near the end see the most keys; a
+  // block-sparse work order lists the units by their visible tiles
   int order, bh;
   grid_order(blockIdx.x, p.BH, p.pairs, &order, &bh);
-  const int pair = p.pairs - 1 - order;
+  const int pair = ordered_tile(p.order, order, p.pairs, p.pairs - 1 - order);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   // query tiles (p.pairs counts the CTAs' units: pairs of tiles, or tiles)
@@ -540,6 +542,8 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
   p.pairs = kTiles == 2 ? (p.T + 1) / 2 : p.T;
+  // the work order holds query tiles at [0, T) and pairs of them at [2T, ...)
+  p.order = p.block_mask && a.tile_order ? a.tile_order + (kTiles == 2 ? 2 * p.T : 0) : nullptr;
   p.BH = BH;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;

@@ -64,6 +64,7 @@ struct FwdArgs {
   int mask_kind;
   const int32_t* kv_len;
   const uint8_t* block_mask;
+  const int32_t* tile_order;  // block-sparse work order (nullptr: the default order)
   int* status;  // 4-int device status block
 };
 
@@ -88,6 +89,7 @@ struct BwdArgs {
   int mask_kind;
   const int32_t* kv_len;
   const uint8_t* block_mask;
+  const int32_t* tile_order;  // block-sparse work order (nullptr: the default order)
   int* status;
 };
 
@@ -112,6 +114,13 @@ cudaError_t launch_bwd_dq64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, 
 cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
+
+// Block-sparse work order (query tiles, key tiles, query-tile pairs, each
+// most work first) of a T x T tile mask: tile_order_len(T) int32.
+constexpr int kMaxTileOrder = 4096;  // = the largest block-mask side the kernels accept
+int tile_order_len(int T);           // 0 when T is out of range
+cudaError_t launch_tile_order(const uint8_t* block_mask, int T, int causal, int32_t* out,
+                              cudaStream_t s);
 inline int tiles_of(int n, int t) { return (n + t - 1) / t; }
 
 // The argument checks of fa_bwd / fa_bwd_ex (bf16), in the same order, short

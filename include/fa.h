@@ -76,7 +76,33 @@ typedef struct {
   const uint8_t* block_mask; /* BLOCK_SPARSE: device uint8 [T*T], T = ceil(N/128)   */
                              /* <= 4096 (N <= 524288; FA_ERR_UNSUPPORTED beyond)    */
   int block_size;            /* BLOCK_SPARSE: tile edge of block_mask, must be 128  */
+  const int32_t* tile_order; /* BLOCK_SPARSE, optional (NULL: the default order):    */
+                             /* the work order fa_block_mask_order wrote for this   */
+                             /* block_mask; device int32, 4-byte aligned            */
 } fa_mask;
+
+/* Work order of a block-sparse mask.  The kernels skip the tiles the mask
+ * hides (summary page, "Extension: block-sparse FlashAttention": only the
+ * nonzero blocks are visited) and give each CTA one tile row or column, so a
+ * row or column that sees far more tiles than the rest (a global token) ends
+ * the kernel alone if the grid takes it last.  This call writes, on `stream`,
+ * fa_block_mask_order_len(T) int32 to tile_order:
+ *   [0, T)              query tiles, most visible key tiles first
+ *   [T, 2T)             key tiles, most query tiles that see them first
+ *   [2T, 2T + (T+1)/2)  pairs of query tiles (2p, 2p+1), most first
+ * counting with the causal restriction when causal = 1; ties keep the lower
+ * index first.  Passed as fa_mask.tile_order, the kernels take their tiles in
+ * that order; every tile is still computed exactly once and the results are
+ * bit-identical to the default order's.  The buffer must be this call's
+ * output (any other permutation of each part is also correct; contents that
+ * are not permutations leave output tiles unwritten or written twice -- the
+ * kernels only clamp entries to [0, T)).  Recompute it when the mask changes;
+ * it costs one small launch per mask.
+ *   block_mask : device uint8 [T*T].   T : 1..4096.   causal : 0 or 1.
+ * Argument errors come back before any CUDA runtime call. */
+int fa_block_mask_order_len(int T); /* 2T + (T+1)/2, or 0 when T is out of range */
+fa_status fa_block_mask_order(const uint8_t* block_mask, int T, int causal, int32_t* tile_order,
+                              void* stream);
 
 /* Forward pass, bf16 in/out.
  *   q, k, v : [B,H,N,d] bf16 inputs.   o : [B,H,N,d] bf16 output.

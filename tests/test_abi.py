@@ -109,6 +109,26 @@ def test_fwd_rejects_bad_masks(fa):
     m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 128))
     assert fwd(fa, mask=m, N=4096 * 128) == 5       # T = 4096: valid (no CUDA here)
     assert fwd(fa, mask=m, N=4096 * 128 + 1) == 2   # T = 4097: beyond the tile bitmap
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 128, FAKE + 2))
+    assert fwd(fa, mask=m) == 3   # misaligned work order
+    assert bwd(fa, mask=m) == 3
+    m = ctypes.pointer(fa.FaMask(fa.FA_MASK_BLOCK_SPARSE, None, FAKE, 128, FAKE))
+    assert fwd(fa, mask=m) == 5   # valid (no CUDA here)
+
+
+def test_block_mask_order_rules(fa):
+    # 2T + ceil(T/2) entries for 1 <= T <= 4096 (the block-mask limit), else 0
+    assert [fa.fa_block_mask_order_len(t) for t in (1, 2, 3, 128, 4096)] == [
+        3, 5, 8, 320, 10240]
+    assert fa.fa_block_mask_order_len(0) == 0 and fa.fa_block_mask_order_len(4097) == 0
+    call = lambda bm=FAKE, T=8, causal=0, out=FAKE: fa.lib.fa_block_mask_order(
+        bm, T, causal, out, None)
+    assert call(bm=0) == 1 and call(out=0) == 1
+    assert call(T=0) == 1 and call(T=4097) == 1 and call(causal=2) == 1
+    assert call(out=FAKE + 2) == 3
+    assert call(T=4096) == 5   # valid: the launch finds no GPU here
+    with pytest.raises(ValueError):
+        fa.make_mask(kv_len=FAKE, tile_order=FAKE)
 
 
 def bwd(fa, **kw):
