@@ -26,6 +26,7 @@ LIB = os.path.join(HERE, "libfa.so")
 SOURCES = [
     "fa_api.cu",
     "fa_fwd_sm103.cu",
+    "fa_fwd64_sm103.cu",
     "fa_bwd_sm103.cu",
     "fa_bwd_dkdv64_sm103.cu",
     "fa_bwd_dq64_sm103.cu",

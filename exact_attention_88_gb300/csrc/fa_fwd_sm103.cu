@@ -562,6 +562,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
+  if (a.d == 64 && !a.drop.t && !a.bias) return launch_fwd64_bf16(a, s);
   return a.d == 64 ? launch_fwd_d<64, 1>(a, s) : launch_fwd_d<128, 2>(a, s);
 }
 

@@ -106,6 +106,7 @@ int* device_status();
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_fwd64_bf16(const FwdArgs& a, cudaStream_t s);  // d = 64, plain
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
