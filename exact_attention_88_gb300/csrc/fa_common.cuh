@@ -526,6 +526,27 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Maximum of 32 scores held as fp32 bit patterns (four independent chains of
+// 3-input maxima), and masking of the keys e >= lim of such a group to -inf.
+__device__ __forceinline__ float max32(const uint32_t* r) {
+  float mx[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    mx[k] = fmaxf(max3(__uint_as_float(r[8 * k]), __uint_as_float(r[8 * k + 1]),
+                       __uint_as_float(r[8 * k + 2])),
+                  max3(__uint_as_float(r[8 * k + 3]), max3(__uint_as_float(r[8 * k + 4]),
+                                                           __uint_as_float(r[8 * k + 5]),
+                                                           __uint_as_float(r[8 * k + 6])),
+                       __uint_as_float(r[8 * k + 7])));
+  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+}
+
+__device__ __forceinline__ void mask32(uint32_t* r, int lim) {  // keys e >= lim are invisible
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (e >= lim) r[e] = 0xff800000u;  // -inf
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
   return *reinterpret_cast<uint32_t*>(&h);

@@ -70,25 +70,6 @@ struct KTiles {
   __device__ int next(int j) const { return bits ? next_tile_bit(bits, j, jend) : j; }
 };
 
-__device__ __forceinline__ float max32(const uint32_t* r) {
-  float mx[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k)
-    mx[k] = fmaxf(max3(__uint_as_float(r[8 * k]), __uint_as_float(r[8 * k + 1]),
-                       __uint_as_float(r[8 * k + 2])),
-                  max3(__uint_as_float(r[8 * k + 3]), max3(__uint_as_float(r[8 * k + 4]),
-                                                           __uint_as_float(r[8 * k + 5]),
-                                                           __uint_as_float(r[8 * k + 6])),
-                       __uint_as_float(r[8 * k + 7])));
-  return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-}
-
-__device__ __forceinline__ void mask32(uint32_t* r, int lim) {  // keys e >= lim are invisible
-#pragma unroll
-  for (int e = 0; e < 32; ++e)
-    if (e >= lim) r[e] = 0xff800000u;  // -inf
-}
-
 // Softmax of this warpgroup's 64 keys of one key tile for this thread's row:
 // keys [0, lim) visible.  tS: the half's S columns, tO: its O columns (lane
 // offset included).
