@@ -47,6 +47,12 @@ SMALL = [
     (2, 2, 512, 128, True, "padding"),
     (1, 2, 640, 64, False, "sparse"),
     (1, 2, 520, 128, True, "sparse"),
+    # d = 64 kernels walk 64-row / 64-key half steps: tails inside either half,
+    # causal with each mask kind
+    (2, 2, 200, 64, False, "none"),       # second half of the last tile partly past N
+    (1, 2, 1000, 64, False, "padding"),
+    (2, 2, 333, 64, True, "padding"),
+    (1, 2, 520, 64, True, "sparse"),
 ]
 
 
@@ -99,6 +105,23 @@ def test_empty_rows(fa):
     o, lse, grads = check_full(fa, case, B, H, N, d, False, "bf16")
     assert torch.all(o[:, :, :128] == 0)
     assert torch.all(torch.isneginf(lse[:, :, :128]))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_unseen_key_tiles_and_all_padding(fa, d):
+    """Key tiles that no query tile sees (an all-zero block-mask column: a dK/dV
+    CTA with no work, dK = dV = 0), and a batch whose keys are all padding
+    (kv_len = 0: O = 0, lse = -inf, no gradient anywhere in that batch)."""
+    B, H, N = 2, 2, 512
+    bm = np.array([[1, 0, 0, 1], [1, 0, 1, 0], [0, 0, 1, 1], [1, 0, 0, 1]], np.uint8)
+    case = random_case(1, H, N, d, seed=41 + d, block_mask=bm)
+    o, lse, (dq, dk, dv) = check_full(fa, case, 1, H, N, d, False, "bf16")
+    assert torch.all(dk[:, :, 128:256] == 0) and torch.all(dv[:, :, 128:256] == 0)
+    case = random_case(B, H, N, d, seed=43 + d, kv_len=np.array([0, 300], np.int32))
+    for causal in (False, True):
+        o, lse, (dq, dk, dv) = check_full(fa, case, B, H, N, d, causal, "bf16")
+        assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+        assert torch.all(dq[0] == 0) and torch.all(dk[0] == 0) and torch.all(dv[0] == 0)
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_causal"])
