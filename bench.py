@@ -319,12 +319,11 @@ def run_gpu(args, rank, world, local_rank):
     kernels = (["mask_order"] if order is not None else []) + [
         "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
     ev = {n: [] for n in kernels}
-    # dK/dV and dQ read the same inputs and write disjoint outputs: in the timed
-    # steps dQ runs on a second stream, so either kernel's last CTAs overlap
-    # the other's; the per-kernel pass runs all four on one stream
-    stream2 = torch.cuda.Stream(dev)
-    ev_pre, ev_dq = torch.cuda.Event(), torch.cuda.Event()
 
+    # A timed step is the public calls: fa_fwd_ex, then fa_bwd_ex (the D
+    # preprocess, then dK/dV and dQ in one launch whose dQ CTAs fill the SMs the
+    # last dK/dV CTAs leave idle).  The per-kernel pass times the same kernels
+    # through the one-step calls, each between CUDA events on the stream.
     def step(record):
         def mark(name, fn):
             if record:
@@ -340,18 +339,15 @@ def run_gpu(args, rank, world, local_rank):
                                                               order, stream))
         mark("fwd", lambda: fa.fa_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, w.causal, mask, opt,
                                          stream))
-        mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
-        dq_stream = stream if record else stream2
         if not record:
-            ev_pre.record(stream)
-            stream2.wait_event(ev_pre)
+            fa.fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N, d, scale, w.causal,
+                         mask, opt, stream)
+            return
+        mark("bwd_preprocess", lambda: fa.fa_bwd_preprocess(o, do, D, B, H, N, d, stream))
         mark("bwd_dkdv", lambda: fa.fa_bwd_dkdv_ex(q, k, v, do, lse, D, dk, dv, B, H, N, d, scale,
                                                    w.causal, mask, opt, stream))
         mark("bwd_dq", lambda: fa.fa_bwd_dq_ex(q, k, v, do, lse, D, dq, B, H, N, d, scale,
-                                               w.causal, mask, opt, dq_stream))
-        if not record:
-            ev_dq.record(stream2)
-            stream.wait_event(ev_dq)  # the next step's forward rewrites o and lse
+                                               w.causal, mask, opt, stream))
 
     dist = None
     if world > 1:
@@ -452,8 +448,9 @@ def run_gpu(args, rank, world, local_rank):
         "dq_roofline": {"kernel": "fa_bwd_dq (S, dP, dQ on tcgen05; S and dP recomputed)",
                         "achieved": round(dq_achieved, 2), "frac": round(dq_achieved / peak, 4),
                         "flops_per_launch": dq_flops},
-        # fwd, preprocess, dK/dV, dQ (+ the two work-order kernels when block-sparse)
-        "gpu_launches": (4 + (2 if order is not None else 0)) * args.steps,
+        # fa_fwd_ex (1), fa_bwd_ex (the preprocess and the combined dK/dV + dQ
+        # kernel: 2), and the work-order kernel when block-sparse (1)
+        "gpu_launches": (3 + (1 if order is not None else 0)) * args.steps,
         "tensor_pipe": tensor_pipe_share(w.name, per_kernel, step_flops, fwd_flops),
         "peak_clocks": peak_clock_note(peaks, clocks),
         "clocks": clocks,
@@ -507,9 +504,9 @@ def peak_clock_note(peaks, clocks):
 def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None, bmask=None,
             order=None):
     """Same metric through the public API with host buffers: every step copies
-    its inputs in from pinned host memory, runs fa_fwd and the three backward
-    steps (dQ on a second stream, as in the device-resident steps) and copies
-    its results (O, lse, dQ, dK, dV) out, all inside the timed region.  Steps
+    its inputs in from pinned host memory, runs fa_fwd_ex and fa_bwd_ex (as in
+    the device-resident steps) and copies its results (O, lse, dQ, dK, dV) out,
+    all inside the timed region.  Steps
     are pipelined over two sets of device buffers: step k+1's inputs go in on
     one copy stream and step k-1's results come out on another while step k
     computes."""
@@ -529,10 +526,8 @@ def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None, bmask=Non
         o["lse"] = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    D = ws[: B * H * N * 4].view(torch.float32)
     s_comp = torch.cuda.current_stream(dev)
-    s_dq, s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_pre, ev_dq = torch.cuda.Event(), torch.cuda.Event()
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
@@ -555,15 +550,8 @@ def run_e2e(fa, torch, dev, case, w, mask, step_flops, args, opt=None, bmask=Non
             fa.fa_block_mask_order(bmask, bmask.shape[0], w.causal, order, s_comp)
         fa.fa_fwd_ex(x["q"], x["k"], x["v"], y["o"], y["lse"], B, H, N, d, w.scale, w.causal, mask,
                      opt, s_comp)
-        fa.fa_bwd_preprocess(y["o"], x["do"], D, B, H, N, d, s_comp)
-        ev_pre.record(s_comp)
-        s_dq.wait_event(ev_pre)
-        fa.fa_bwd_dkdv_ex(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dk"], y["dv"], B, H, N,
-                          d, w.scale, w.causal, mask, opt, s_comp)
-        fa.fa_bwd_dq_ex(x["q"], x["k"], x["v"], x["do"], y["lse"], D, y["dq"], B, H, N, d,
-                        w.scale, w.causal, mask, opt, s_dq)
-        ev_dq.record(s_dq)
-        s_comp.wait_event(ev_dq)
+        fa.fa_bwd_ex(x["q"], x["k"], x["v"], y["o"], x["do"], y["lse"], y["dq"], y["dk"], y["dv"],
+                     ws, ws_bytes, B, H, N, d, w.scale, w.causal, mask, opt, s_comp)
         comp_done[k % 2].record(s_comp)
 
     def copy_out(k):

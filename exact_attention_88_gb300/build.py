@@ -31,13 +31,15 @@ SOURCES = [
     "fa_bwd_dkdv64_sm103.cu",
     "fa_bwd_dq64_sm103.cu",
     "fa_bwd_dq_sm103.cu",
+    "fa_bwd_pair_sm103.cu",
     "fa_bwd_aux.cu",
     "fa_fp32.cu",
     "fa_probe.cu",
     "fa_noalloc.cu",
     "fa_tile_order.cu",
 ]
-HEADERS = ["fa_common.cuh", "fa_internal.h"]
+HEADERS = ["fa_common.cuh", "fa_internal.h", "fa_bwd_dkdv.cuh", "fa_bwd_dkdv64.cuh", "fa_bwd_dq.cuh",
+           "fa_bwd_dq64.cuh"]
 DIAG_SOURCES = [os.path.join("diag", "fa_diag.cu")]
 DIAG_LIB = os.path.join(HERE, "libfa_diag.so")
 

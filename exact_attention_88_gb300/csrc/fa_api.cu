@@ -163,6 +163,13 @@ bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B,
   return r == CUDA_SUCCESS;
 }
 
+bool encode_bwd_maps(const BwdArgs& a, CUtensorMap m[4]) {
+  return encode_bhnd_map(&m[0], a.q, a.lq, a.B, a.H, a.N, a.d, 128) &&
+         encode_bhnd_map(&m[1], a.k, a.lk, a.B, a.H, a.N, a.d, 128) &&
+         encode_bhnd_map(&m[2], a.v, a.lv, a.B, a.H, a.N, a.d, 128) &&
+         encode_bhnd_map(&m[3], a.dO, a.ldo, a.B, a.H, a.N, a.d, 128);
+}
+
 int* device_status() {
   static int* ptrs[kMaxDevices] = {nullptr};
   static std::mutex mu;
@@ -361,8 +368,8 @@ fa_status fa_bwd_ex(const void* q, const void* k, const void* v, const void* o, 
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = launched(launch_bwd_preprocess(a, s));
-  if (st == FA_OK) st = launched(launch_bwd_dkdv_bf16(a, s));
-  if (st == FA_OK) st = launched(launch_bwd_dq_bf16(a, s));
+  // dK/dV and dQ in one launch, their CTAs interleaved
+  if (st == FA_OK) st = launched(launch_bwd_pair_bf16(a, s));
   return st;
 }
 

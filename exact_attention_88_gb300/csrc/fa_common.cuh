@@ -13,6 +13,9 @@
 
 namespace fa {
 
+constexpr float kLog2e = 1.4426950408889634f;  // scores in base 2: exp(x) = 2^(x log2 e)
+constexpr float kLn2 = 0.6931471805599453f;
+
 // ---------------------------------------------------------------------------
 // status words.  Every kernel gets a pointer to a 4-int status block in device
 // memory: [0] error code (0 = ok, 6 = timeout), [1] site id, [2] block, [3] aux.
@@ -153,6 +156,13 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, i
 // dependent global loads (one per skipped tile).
 // ---------------------------------------------------------------------------
 constexpr int kMaskBitmapWords = 128;  // tiles per bitmap: 4096 (N <= 524288)
+
+// The block-mask bitmap of a CTA (its tile row or column).  One array per
+// kernel: a kernel that runs one of several CTA bodies shares it between them.
+__device__ __forceinline__ uint32_t* tile_mask_bitmap() {
+  __shared__ uint32_t bits[kMaskBitmapWords];
+  return bits;
+}
 
 // bits[t / 32] bit t % 32 = (first[t * stride] != 0), t < T.  Every thread of
 // the CTA takes part (whole warps); a __syncthreads must follow before use.

@@ -45,8 +45,6 @@
 namespace fa {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P~ stays below 2^8
 
 template <int D, int kTiles>

@@ -100,6 +100,10 @@ struct BwdArgs {
 bool encode_bhnd_map(CUtensorMap* map, const void* base, const Layout& l, int B, int H, int N,
                      int d, int box_rows);
 
+// The four maps every backward kernel reads (Q, K, V, dO; box 128 rows), in
+// that order; false when one cannot be encoded.
+bool encode_bwd_maps(const BwdArgs& a, CUtensorMap m[4]);
+
 // Device address of the status block of the current device (no allocation:
 // it is a __device__ variable), or nullptr on failure.
 int* device_status();
@@ -112,6 +116,7 @@ cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
 cudaError_t launch_bwd_dq_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dq64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
+cudaError_t launch_bwd_pair_bf16(const BwdArgs& a, cudaStream_t s);  // dK/dV and dQ, one launch
 cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
