@@ -48,7 +48,6 @@
 namespace fa {
 namespace {
 
-
 template <int D>
 struct BwdCfg {
   static constexpr int kTileBytes = 128 * D * 2;
@@ -563,7 +562,6 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
-
 
 // The kernel parameters of a call (host).
 inline BwdParams make_dkdv_params(const BwdArgs& a) {

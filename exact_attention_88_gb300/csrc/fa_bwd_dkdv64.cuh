@@ -40,7 +40,6 @@
 namespace fa {
 namespace {
 
-
 struct Bwd64Cfg {
   static constexpr int D = 64;
   static constexpr int kTileBytes = 128 * D * 2;
@@ -458,7 +457,6 @@ __device__ __forceinline__ void dkdv64_cta(const CUtensorMap& tmQ, const CUtenso
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
-
 
 // The kernel parameters of a call (host).
 inline Bwd64Params make_dkdv64_params(const BwdArgs& a) {

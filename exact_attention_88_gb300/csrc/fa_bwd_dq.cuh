@@ -39,7 +39,6 @@
 namespace fa {
 namespace {
 
-
 template <int D>
 struct DqCfg {
   static constexpr int kTileBytes = 128 * D * 2;
@@ -419,7 +418,6 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
-
 
 // The kernel parameters of a call (host).
 inline DqParams make_dq_params(const BwdArgs& a) {

@@ -41,7 +41,6 @@
 namespace fa {
 namespace {
 
-
 struct Dq64Cfg {
   static constexpr int D = 64;
   static constexpr int kTileBytes = 128 * D * 2;
@@ -381,7 +380,6 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
-
 
 // The kernel parameters of a call (host).
 inline Dq64Params make_dq64_params(const BwdArgs& a) {
