@@ -242,7 +242,7 @@ __device__ __forceinline__ uint32_t keep_bits_of_row(const DropParams& d, uint32
                                                      int key0) {
   uint32_t bits = 0;
 #pragma unroll 2
-  for (int g = 0; g < 4; ++g) {  // two calls in flight: few registers
+  for (int g = 0; g < 4; ++g) {  // two calls in flight (four: slower)
     const uint4 w = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
     bits |= keep_bits8(w, d.t) << (8 * g);
   }
@@ -258,8 +258,8 @@ __device__ __forceinline__ uint32_t keep_bits_of_key(const DropParams& d, uint32
                                                      int q0) {
   const int lane = threadIdx.x & 31, m = key & 7;
   uint32_t mine = 0;  // byte r: the group's keys for row q0 + (lane % 8) + 8r
-#pragma unroll 1
-  for (int r = 0; r < 4; ++r) {  // one call at a time: few registers
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {  // four independent calls in flight
     const uint4 w = philox4x32_10((uint32_t)key >> 3, (uint32_t)(q0 + (lane & 7) + 8 * r), bh,
                                   d.offset, d.k0, d.k1);
     mine |= keep_bits8(w, d.t) << (8 * r);
