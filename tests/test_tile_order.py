@@ -32,7 +32,8 @@ def expected_order(bm, causal):
 
 
 MASKS = [("random", 1), ("random", 5), ("random", 128), ("random", 130), ("local_global", 128),
-         ("butterfly", 64), ("strided", 37), ("local", 512)]
+         ("butterfly", 64), ("strided", 37), ("local", 512),
+         ("random", 4096), ("local_global", 4095)]  # the largest side: 72 KB of shared memory
 
 
 @pytest.mark.parametrize("pattern,T", MASKS)
