@@ -318,6 +318,9 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
       const bool partial = lim < 32;
       uint32_t rs_all[32];
       FA_TMEM_LD32_SYNC(tS, rs_all);
+      // S_u is in registers: S_{u+1} may overwrite it while the exponentials run
+      tc_fence_before();
+      mbar_arrive_warp(&s_free);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t* rs = rs_all + 16 * h;
@@ -329,9 +332,6 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
           pf[16 * h + e + 1] = ex2(t.y);
         }
       }
-      // S_u has been read: S_{u+1} may overwrite it
-      tc_fence_before();
-      mbar_arrive_warp(&s_free);
       if (partial) {
 #pragma unroll
         for (int e = 0; e < 32; ++e)

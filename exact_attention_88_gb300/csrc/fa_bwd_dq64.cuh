@@ -307,6 +307,9 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
         if (p.causal) lim = min(lim, q - key0 + 1);
         uint32_t rs[32];
         FA_TMEM_LD32_SYNC(tmem + C::kColS + lane_off + col0, rs);
+        // S_s is in registers: S_{s+1} may overwrite it while the exponentials run
+        tc_fence_before();
+        mbar_arrive_warp(&s_free);
         float pf[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -315,9 +318,6 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
           pf[e] = ex2(t.x);
           pf[e + 1] = ex2(t.y);
         }
-        // S_s has been read: S_{s+1} may overwrite it
-        tc_fence_before();
-        mbar_arrive_warp(&s_free);
         if (lim < 32) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
