@@ -70,6 +70,7 @@ struct Bwd64Params {
   const uint8_t* block_mask;
   const int32_t* order;  // block-sparse work order (key tiles) or nullptr
   int H, N, T, BH;
+  int group;  // heads per group of the grid order
   float scale, scale_log2;
   int causal;
   int* status;
@@ -126,7 +127,7 @@ __device__ __forceinline__ void dkdv64_cta(const CUtensorMap& tmQ, const CUtenso
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int kt, bh;  // key tile (causal: low tiles have the most work: first)
-  grid_order(cta, p.BH, p.T, &kt, &bh);
+  grid_order(cta, p.BH, p.T, p.group, &kt, &bh);
   kt = ordered_tile(p.order, kt, p.T, kt);  // block-sparse work order: by query tiles seen
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
@@ -473,6 +474,7 @@ inline Bwd64Params make_dkdv64_params(const BwdArgs& a) {
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
   p.BH = a.B * a.H;
+  p.group = grid_group_heads(a.B, a.H, a.N, a.d, a.causal);
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;

@@ -71,6 +71,7 @@ struct DqParams {
   const uint8_t* block_mask;
   const int32_t* order;  // block-sparse work order (query tiles) or nullptr
   int H, N, T, BH;
+  int group;  // heads per group of the grid order
   float scale, scale_log2;
   int causal;
   int* status;
@@ -109,7 +110,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int order, bh;
-  grid_order(cta, p.BH, p.T, &order, &bh);
+  grid_order(cta, p.BH, p.T, p.group, &order, &bh);
   // causal: the last query tiles see the most keys: first; a block-sparse
   // work order lists the query tiles by their visible key tiles
   const int qi = ordered_tile(p.order, order, p.T, p.T - 1 - order);
@@ -435,6 +436,7 @@ inline DqParams make_dq_params(const BwdArgs& a) {
   p.N = a.N;
   p.T = tiles_of(a.N, 128);
   p.BH = a.B * a.H;
+  p.group = grid_group_heads(a.B, a.H, a.N, a.d, a.causal);
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;

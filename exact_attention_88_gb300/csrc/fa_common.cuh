@@ -300,12 +300,12 @@ __device__ __forceinline__ void load_bias_row(const float* brow, int k0, int n_k
 
 // ---------------------------------------------------------------------------
 // Grid order: CTA lin -> (work-order index t, head bh) with the heads taken
-// kGroupHeads at a time, so that the CTAs resident at once share the K / V
-// (or Q / dO) tiles of a few heads in L2 instead of all of them; within a group
+// `group` at a time, so that the CTAs resident at once share the K / V (or
+// Q / dO) tiles of a few heads in L2 instead of all of them; within a group
 // the order index runs slowest (t = 0 first: the callers put the heaviest
-// tiles there).  A last, smaller group takes the remaining heads.
+// tiles there).  A last, smaller group takes the remaining heads.  The host
+// picks the group (grid_group_heads): all heads when the inputs fit in L2.
 // ---------------------------------------------------------------------------
-constexpr int kGroupHeads = 8;
 
 // Tile taken by order index t: entry t of a block-sparse work order when the
 // caller gives one (clamped to [0, n)), else `fallback`.
@@ -313,13 +313,13 @@ __device__ __forceinline__ int ordered_tile(const int32_t* order, int t, int n, 
   return order ? min(max(__ldg(order + t), 0), n - 1) : fallback;
 }
 
-__device__ __forceinline__ void grid_order(int lin, int BH, int nt, int* t, int* bh) {
-  const int per_group = kGroupHeads * nt;
+__device__ __forceinline__ void grid_order(int lin, int BH, int nt, int group, int* t, int* bh) {
+  const int per_group = group * nt;
   const int g = lin / per_group;
   const int r = lin - g * per_group;
-  const int gh = min(kGroupHeads, BH - g * kGroupHeads);  // heads in this group
+  const int gh = min(group, BH - g * group);  // heads in this group
   *t = r / gh;
-  *bh = g * kGroupHeads + (r - *t * gh);
+  *bh = g * group + (r - *t * gh);
 }
 
 // One arrival for the whole warp, made by lane 0 once every lane has got

@@ -54,6 +54,7 @@ struct Fwd64Params {
   const uint8_t* block_mask;
   const int32_t* order;  // block-sparse work order (query tiles) or nullptr
   int H, N, T, BH;
+  int group;  // heads per group of the grid order
   float scale_log2;
   int causal;
   int* status;
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(Fwd64Cfg::kThreads, 2)
   // causal: the last query tiles see the most keys: first; a block-sparse work
   // order lists the query tiles by their visible key tiles
   int order, bh;
-  grid_order(blockIdx.x, p.BH, p.T, &order, &bh);
+  grid_order(blockIdx.x, p.BH, p.T, p.group, &order, &bh);
   const int qi = ordered_tile(p.order, order, p.T, p.T - 1 - order);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
@@ -367,6 +368,7 @@ cudaError_t launch_fwd64_bf16(const FwdArgs& a, cudaStream_t s) {
   p.T = tiles_of(a.N, 128);
   p.order = p.block_mask ? a.tile_order : nullptr;  // query tiles at [0, T)
   p.BH = BH;
+  p.group = grid_group_heads(a.B, a.H, a.N, a.d, a.causal);
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;

@@ -83,6 +83,7 @@ struct FwdParams {
   const uint8_t* block_mask;
   const int32_t* order;  // block-sparse work order of the units (pairs or tiles), or nullptr
   int H, N, T, BH, pairs;
+  int group;  // heads per group of the grid order
   float scale_log2;
   int causal;
   int* status;
@@ -264,7 +265,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTiles>::kThreads, FwdCfg<D, kTiles>
   // heaviest pairs first: causal rows near the end see the most keys; a
   // block-sparse work order lists the units by their visible tiles
   int order, bh;
-  grid_order(blockIdx.x, p.BH, p.pairs, &order, &bh);
+  grid_order(blockIdx.x, p.BH, p.pairs, p.group, &order, &bh);
   const int pair = ordered_tile(p.order, order, p.pairs, p.pairs - 1 - order);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
@@ -543,6 +544,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   // the work order holds query tiles at [0, T) and pairs of them at [2T, ...)
   p.order = p.block_mask && a.tile_order ? a.tile_order + (kTiles == 2 ? 2 * p.T : 0) : nullptr;
   p.BH = BH;
+  p.group = grid_group_heads(a.B, a.H, a.N, a.d, a.causal);
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
