@@ -39,6 +39,7 @@ SOURCES = [
     "fa_tile_order.cu",
 ]
 HEADERS = ["fa_common.cuh", "fa_internal.h", "fa_bwd_dkdv.cuh", "fa_bwd_dkdv64.cuh", "fa_bwd_dq.cuh",
+           "fa_bwd_persist.cuh",
            "fa_bwd_dq64.cuh"]
 DIAG_SOURCES = [os.path.join("diag", "fa_diag.cu")]
 DIAG_LIB = os.path.join(HERE, "libfa_diag.so")

@@ -247,11 +247,17 @@ static fa_status fill_bwd_common(BwdArgs* a, int B, int H, int N, int d, float s
   return FA_OK;
 }
 
+// The workspace: D (fp32 [B,H,N], padded to 256 bytes), then the work
+// counter of the persistent backward kernel.
+constexpr size_t kSchedBytes = 256;
+
 static fa_status split_workspace(BwdArgs* a, void* ws, size_t ws_bytes) {
   if (!ws) return FA_ERR_WORKSPACE;
   if (!aligned16(ws)) return FA_ERR_ALIGNMENT;
-  if (ws_bytes < round256((size_t)a->B * a->H * a->N * sizeof(float))) return FA_ERR_WORKSPACE;
+  const size_t d_bytes = round256((size_t)a->B * a->H * a->N * sizeof(float));
+  if (ws_bytes < d_bytes + kSchedBytes) return FA_ERR_WORKSPACE;
   a->D = static_cast<float*>(ws);
+  a->sched = reinterpret_cast<int*>(static_cast<char*>(ws) + d_bytes);
   return FA_OK;
 }
 
@@ -316,7 +322,7 @@ const char* fa_status_string(fa_status s) {
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d) != FA_OK) return 0;
-  return round256((size_t)B * H * N * sizeof(float));
+  return round256((size_t)B * H * N * sizeof(float)) + kSchedBytes;
 }
 
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -1,5 +1,7 @@
 // Memory-bound step ahead of the backward kernels:
 //   preprocess : D_i = sum_c dO_ic * O_ic (fp32)
+// It also zeroes the work counter of the backward kernel that follows it on
+// the stream (when the call has one).
 // It streams O and dO once with 16-byte accesses.  A block covers kUnroll
 // slabs of consecutive rows and issues every load of its rows before it
 // reduces any, so that each thread keeps 2 kUnroll loads in flight (one load
@@ -24,8 +26,9 @@ constexpr int kUnroll = 4;
 template <int D, bool kDense>
 __global__ void __launch_bounds__(kPreThreads) bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-    float* __restrict__ Dout, long long rows, int H, int N, Layout lo, Layout ldo) {
+    float* __restrict__ Dout, long long rows, int H, int N, Layout lo, Layout ldo, int* sched) {
   constexpr int G = D / 8;                  // lanes per row (8 or 16)
+  if (sched && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   constexpr int R = kPreThreads / G;        // rows per slab
   const int g = threadIdx.x % G;
   const long long row0 = (long long)blockIdx.x * R * kUnroll + threadIdx.x / G;
@@ -80,7 +83,7 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const auto* o = static_cast<const __nv_bfloat16*>(a.o);
   const auto* dO = static_cast<const __nv_bfloat16*>(a.dO);
   auto go = [&](auto kernel) {
-    kernel<<<grid, kPreThreads, 0, s>>>(o, dO, a.D, rows, a.H, a.N, a.lo, a.ldo);
+    kernel<<<grid, kPreThreads, 0, s>>>(o, dO, a.D, rows, a.H, a.N, a.lo, a.ldo, a.sched);
   };
   if (a.d == 64)
     dense ? go(bwd_preprocess_kernel<64, true>) : go(bwd_preprocess_kernel<64, false>);

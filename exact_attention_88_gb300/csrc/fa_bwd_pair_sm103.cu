@@ -10,10 +10,14 @@
 // The two bodies of a pair have the same
 // thread count, TMEM allocation and CTAs per SM; the dynamic shared memory is
 // the larger of the two.
+// At d = 128 without a block mask, key padding, dropout or a bias, the dQ
+// part is one persistent CTA per SM that takes query tiles one after another
+// (fa_bwd_persist.cuh): long causal 2.525 against 2.552-2.562 ms.
 #include "fa_bwd_dkdv.cuh"
 #include "fa_bwd_dkdv64.cuh"
 #include "fa_bwd_dq.cuh"
 #include "fa_bwd_dq64.cuh"
+#include "fa_bwd_persist.cuh"
 
 namespace fa {
 namespace {
@@ -57,6 +61,44 @@ __global__ void __launch_bounds__(Bwd64Cfg::kThreads, 2)
     dq64_cta(tmQ, tmK, tmV, tmDO, pq, idx);
 }
 
+// Persistent dQ: the first n0 CTAs are the one-per-unit dK/dV CTAs; the last
+// gridDim - n0 CTAs each hold 512 TMEM columns and take dQ units from the
+// counter (CTA x starts with unit x) until none is left.
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    fa_bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                          const BwdParams pk, const DqParams pq, int* counter) {
+  const int n0 = pk.T * pk.BH, n = n0 + pq.T * pq.BH;
+  if ((int)blockIdx.x < n0) {
+    dkdv_cta<D, false>(tmQ, tmK, tmV, tmDO, pk, blockIdx.x);
+    return;
+  }
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5;
+  if (warp == BwdCfg<D>::kMathWarps + 1) tmem_alloc(&tmem_slot, BwdCfg<D>::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  dq_persist<D>(tmQ, tmK, tmV, tmDO, pq, tmem, blockIdx.x, n0, n, counter);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == BwdCfg<D>::kMathWarps + 1) {
+    __syncwarp();
+    tmem_dealloc(tmem, BwdCfg<D>::kTmemCols);
+  }
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return sms;
+}
+
 template <class Kernel, class PK, class PQ>
 cudaError_t launch_pair(Kernel kernel, int threads, int smem, const CUtensorMap* m, const PK& pk,
                         const PQ& pq, cudaStream_t s) {
@@ -78,6 +120,21 @@ cudaError_t launch_pair_d(const BwdArgs& a, const CUtensorMap* m, cudaStream_t s
 cudaError_t launch_bwd_pair_bf16(const BwdArgs& a, cudaStream_t s) {
   CUtensorMap m[4];
   if (!encode_bwd_maps(a, m)) return cudaErrorInvalidValue;
+  if (a.d == 128 && !a.drop.t && !a.bias && a.mask_kind == FA_MASK_NONE && a.sched) {
+    const BwdParams pk = make_dkdv_params(a);
+    const DqParams pq = make_dq_params(a);
+    const int units = pk.T * pk.BH + pq.T * pq.BH;
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    const int smem = max(BwdCfg<128>::kSmem, DqCfg<128>::kSmem);
+    auto kernel = fa_bwd_persist_kernel<128>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int n0 = pk.T * pk.BH;
+    kernel<<<n0 + min(units - n0, sms), BwdCfg<128>::kThreads, smem, s>>>(m[0], m[1], m[2], m[3],
+                                                                        pk, pq, a.sched);
+    return cudaGetLastError();
+  }
   if (a.d == 64 && !a.drop.t && !a.bias)
     return launch_pair(fa_bwd64_pair_kernel, Bwd64Cfg::kThreads, max(Bwd64Cfg::kSmem, Dq64Cfg::kSmem),
                        m, make_dkdv64_params(a), make_dq64_params(a), s);

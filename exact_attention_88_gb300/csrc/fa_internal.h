@@ -76,6 +76,7 @@ struct BwdArgs {
   const void* dO;
   const float* lse;
   float* D;  // fp32 [B,H,N]
+  int* sched;  // work counter of the persistent backward (in the workspace), or nullptr
   void* dq;
   void* dk;
   void* dv;

@@ -116,7 +116,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int N, int d, float scale, int causal, const fa_mask* mask, void* stream);
 
 /* Bytes of device workspace fa_bwd / fa_bwd_fp32 need: D (fp32 [B,H,N]),
- * padded to 256 bytes.  0 on bad sizes. */
+ * padded to 256 bytes, then 256 bytes for the counter from which the backward
+ * kernel's CTAs take their units of work.  0 on bad sizes. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /* Backward pass, bf16.  Given the forward's inputs, its outputs o and lse,

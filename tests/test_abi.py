@@ -59,7 +59,8 @@ def test_workspace_size(fa):
     B, H, N, d = 2, 3, 1000, 128
     rows = B * H * N
     r256 = lambda x: (x + 255) // 256 * 256
-    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4)
+    # D (fp32 per row, padded to 256 bytes), then 256 bytes for the work counter
+    assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * 4) + 256
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
     assert fa.fa_bwd_workspace_size(1, 1, 1, 96) == 0
 
@@ -142,6 +143,7 @@ def bwd(fa, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), 1), (dict(dO=0), 1), (dict(dq=FAKE + 4), 3), (dict(d=32), 2),
     (dict(ws=0), 4), (dict(ws_bytes=100), 4), (dict(ws=FAKE + 8), 3), (dict(scale=-0.1), 1),
+    (dict(ws_bytes=512), 4),  # room for D (128 rows) but not for the work counter
 ])
 def test_bwd_rejects_bad_arguments(fa, kw, code):
     assert bwd(fa, **kw) == code
