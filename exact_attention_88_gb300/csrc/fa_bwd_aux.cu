@@ -28,6 +28,8 @@ __global__ void __launch_bounds__(kPreThreads) bwd_preprocess_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
     float* __restrict__ Dout, long long rows, int H, int N, Layout lo, Layout ldo, int* sched) {
   constexpr int G = D / 8;                  // lanes per row (8 or 16)
+  pdl_wait();  // the kernel ahead on the stream (the forward) is done
+  pdl_launch_dependents();
   if (sched && blockIdx.x == 0 && threadIdx.x == 0) *sched = 0;
   constexpr int R = kPreThreads / G;        // rows per slab
   const int g = threadIdx.x % G;
@@ -83,13 +85,12 @@ cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s) {
   const auto* o = static_cast<const __nv_bfloat16*>(a.o);
   const auto* dO = static_cast<const __nv_bfloat16*>(a.dO);
   auto go = [&](auto kernel) {
-    kernel<<<grid, kPreThreads, 0, s>>>(o, dO, a.D, rows, a.H, a.N, a.lo, a.ldo, a.sched);
+    return launch_pdl(kernel, dim3(grid), dim3(kPreThreads), 0, s, o, dO, a.D, rows, a.H, a.N, a.lo,
+                      a.ldo, a.sched);
   };
   if (a.d == 64)
-    dense ? go(bwd_preprocess_kernel<64, true>) : go(bwd_preprocess_kernel<64, false>);
-  else
-    dense ? go(bwd_preprocess_kernel<128, true>) : go(bwd_preprocess_kernel<128, false>);
-  return cudaGetLastError();
+    return dense ? go(bwd_preprocess_kernel<64, true>) : go(bwd_preprocess_kernel<64, false>);
+  return dense ? go(bwd_preprocess_kernel<128, true>) : go(bwd_preprocess_kernel<128, false>);
 }
 
 }  // namespace fa

@@ -191,6 +191,7 @@ __device__ __forceinline__ void dkdv_cta(const CUtensorMap& tmQ, const CUtensorM
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();  // TMEM held: the next kernel may become resident
 
   if (warp == C::kMathWarps) {
     // ------------------------------------------------------------ producer

@@ -146,6 +146,7 @@ __device__ __forceinline__ void dq_cta(const CUtensorMap& tmQ, const CUtensorMap
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();  // TMEM held: the next kernel may become resident
   const int jfirst = ktiles.next(0);  // after the barrier: the bitmap is complete
   const bool any = jfirst < ktiles.jend;
 

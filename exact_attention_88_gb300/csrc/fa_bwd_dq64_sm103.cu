@@ -10,6 +10,7 @@ __global__ void __launch_bounds__(Dq64Cfg::kThreads, 2)
     fa_bwd_dq64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const Dq64Params p) {
+  pdl_wait();
   dq64_cta(tmQ, tmK, tmV, tmDO, p, blockIdx.x);
 }
 
@@ -23,8 +24,8 @@ cudaError_t launch_bwd_dq64_bf16(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(fa_bwd_dq64_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_bwd_dq64_kernel<<<p.T * p.BH, C::kThreads, C::kSmem, s>>>(m[0], m[1], m[2], m[3], p);
-  return cudaGetLastError();
+  return launch_pdl(fa_bwd_dq64_kernel, dim3(p.T * p.BH), dim3(C::kThreads), C::kSmem, s, m[0],
+                    m[1], m[2], m[3], p);
 }
 
 }  // namespace fa

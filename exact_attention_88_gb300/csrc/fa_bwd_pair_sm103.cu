@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams pk, const DqParams pq) {
+  pdl_wait();
   int kind, idx;
   split_grid(blockIdx.x, pk.T * pk.BH, pq.T * pq.BH, &kind, &idx);
   if (kind == 0)
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(Bwd64Cfg::kThreads, 2)
     fa_bwd64_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const Bwd64Params pk, const Dq64Params pq) {
+  pdl_wait();
   int kind, idx;
   split_grid(blockIdx.x, pk.T * pk.BH, pq.T * pq.BH, &kind, &idx);
   if (kind == 0)
@@ -69,6 +71,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                           const BwdParams pk, const DqParams pq, int* counter) {
+  pdl_wait();
   const int n0 = pk.T * pk.BH, n = n0 + pq.T * pq.BH;
   if ((int)blockIdx.x < n0) {
     dkdv_cta<D, false>(tmQ, tmK, tmV, tmDO, pk, blockIdx.x);
@@ -81,6 +84,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();  // TMEM held: the next kernel may become resident
   dq_persist<D>(tmQ, tmK, tmV, tmDO, pq, tmem, blockIdx.x, n0, n, counter);
   tc_fence_before();
   __syncthreads();
@@ -104,8 +108,8 @@ cudaError_t launch_pair(Kernel kernel, int threads, int smem, const CUtensorMap*
                         const PQ& pq, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<pk.T * pk.BH + pq.T * pq.BH, threads, smem, s>>>(m[0], m[1], m[2], m[3], pk, pq);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(pk.T * pk.BH + pq.T * pq.BH), dim3(threads), smem, s, m[0], m[1],
+                    m[2], m[3], pk, pq);
 }
 
 template <int D>
@@ -131,9 +135,8 @@ cudaError_t launch_bwd_pair_bf16(const BwdArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int n0 = pk.T * pk.BH;
-    kernel<<<n0 + min(units - n0, sms), BwdCfg<128>::kThreads, smem, s>>>(m[0], m[1], m[2], m[3],
-                                                                        pk, pq, a.sched);
-    return cudaGetLastError();
+    return launch_pdl(kernel, dim3(n0 + min(units - n0, sms)), dim3(BwdCfg<128>::kThreads), smem, s,
+                      m[0], m[1], m[2], m[3], pk, pq, a.sched);
   }
   if (a.d == 64 && !a.drop.t && !a.bias)
     return launch_pair(fa_bwd64_pair_kernel, Bwd64Cfg::kThreads, max(Bwd64Cfg::kSmem, Dq64Cfg::kSmem),

@@ -11,6 +11,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
+  pdl_wait();
   dkdv_cta<D, kExtra>(tmQ, tmK, tmV, tmDO, p, blockIdx.x);
 }
 
@@ -24,8 +25,8 @@ cudaError_t launch_dkdv_d(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  kernel<<<p.T * p.BH, C::kThreads, C::kSmem, s>>>(m[0], m[1], m[2], m[3], p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(p.T * p.BH), dim3(C::kThreads), C::kSmem, s, m[0], m[1], m[2], m[3],
+                    p);
 }
 
 }  // namespace

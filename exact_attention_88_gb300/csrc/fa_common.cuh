@@ -334,6 +334,19 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with it (launch_pdl) may
+// be resident before the kernel ahead of it on the stream has finished:
+// pdl_wait() returns once that kernel has completed and its memory is
+// visible, so every kernel calls it before its first global-memory access.
+// pdl_launch_dependents() lets the kernel behind it become resident once
+// every CTA of this one has called it (or exited); a CTA calls it after its
+// TMEM allocation, so that a waiting dependent never holds TMEM columns that
+// a CTA of this kernel still has to allocate.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA)
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

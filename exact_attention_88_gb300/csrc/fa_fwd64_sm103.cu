@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(Fwd64Cfg::kThreads, 2)
   __shared__ float s_m[2][128], s_l[2][128];  // each half's final statistics, by row
   __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask row qi
 
+  pdl_wait();  // the kernel ahead on the stream is done (it may write our inputs)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // causal: the last query tiles see the most keys: first; a block-sparse work
   // order lists the query tiles by their visible key tiles
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(Fwd64Cfg::kThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();  // TMEM held: the next kernel may become resident
   const int jfirst = tiles.next(0);  // after the barrier: the bitmap is complete
 
   if (warp == C::kProducerWarp) {
@@ -375,8 +377,7 @@ cudaError_t launch_fwd64_bf16(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e =
       cudaFuncSetAttribute(fa_fwd64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  fa_fwd64_kernel<<<p.T * BH, C::kThreads, C::kSmem, s>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  return launch_pdl(fa_fwd64_kernel, dim3(p.T * BH), dim3(C::kThreads), C::kSmem, s, mq, mk, mv, p);
 }
 
 }  // namespace fa

@@ -261,6 +261,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTiles>::kThreads, FwdCfg<D, kTiles>
   __shared__ int abort_flag;
   __shared__ uint32_t mask_bits[2][kMaskBitmapWords];  // block-mask rows qa, qb
 
+  pdl_wait();  // the kernel ahead on the stream is done (it may write our inputs)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // heaviest pairs first: causal rows near the end see the most keys; a
   // block-sparse work order lists the units by their visible tiles
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(FwdCfg<D, kTiles>::kThreads, FwdCfg<D, kTiles>
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  pdl_launch_dependents();  // TMEM held: the next kernel may become resident
 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -555,8 +557,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.pairs * BH);
-  kernel<<<grid, C::kThreads, C::kSmem, s>>>(mq, mk, mv, p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, dim3(C::kThreads), C::kSmem, s, mq, mk, mv, p);
 }
 
 }  // namespace

@@ -109,6 +109,25 @@ bool encode_bwd_maps(const BwdArgs& a, CUtensorMap m[4]);
 // it is a __device__ variable), or nullptr on failure.
 int* device_status();
 
+// Launch with programmatic stream serialization: the kernel's CTAs may become
+// resident while the kernel ahead of it on the stream finishes; the kernel
+// waits for that one (pdl_wait) before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd64_bf16(const FwdArgs& a, cudaStream_t s);  // d = 64, plain

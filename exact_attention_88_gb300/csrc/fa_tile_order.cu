@@ -99,6 +99,8 @@ template <bool kVec>
 __global__ void __launch_bounds__(kOrderThreads)
     tile_order_kernel(const uint8_t* __restrict__ bm, int T, int causal, int32_t* __restrict__ out) {
   extern __shared__ int cnt[];  // rows [0, T), columns [T, 2T), pairs [2T, 2T + P), bins
+  pdl_wait();  // the kernel ahead on the stream is done (it may read `out`)
+  pdl_launch_dependents();
   const int P = (T + 1) / 2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int e = threadIdx.x; e < 2 * T; e += blockDim.x) cnt[e] = 0;
@@ -185,8 +187,7 @@ cudaError_t launch_tile_order(const uint8_t* block_mask, int T, int causal, int3
   auto kernel = vec ? tile_order_kernel<true> : tile_order_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kernel<<<1, kOrderThreads, smem, s>>>(block_mask, T, causal, out);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(1), dim3(kOrderThreads), (size_t)smem, s, block_mask, T, causal, out);
 }
 
 }  // namespace fa
