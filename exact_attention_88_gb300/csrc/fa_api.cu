@@ -280,6 +280,17 @@ static fa_status fill_bwd_full(BwdArgs* a, const void* q, const void* k, const v
   return attach_status(a) ? FA_OK : FA_ERR_CUDA;
 }
 
+int fa::device_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cached[dev] = sms;
+  return sms;
+}
+
 // Text of the last CUDA error a call of this thread failed with.
 static thread_local const char* t_last_cuda_error = "no CUDA error";
 

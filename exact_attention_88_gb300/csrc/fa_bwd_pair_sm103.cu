@@ -95,14 +95,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-int sm_count() {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return 0;
-  return sms;
-}
-
 template <class Kernel, class PK, class PQ>
 cudaError_t launch_pair(Kernel kernel, int threads, int smem, const CUtensorMap* m, const PK& pk,
                         const PQ& pq, cudaStream_t s) {
@@ -128,7 +120,7 @@ cudaError_t launch_bwd_pair_bf16(const BwdArgs& a, cudaStream_t s) {
     const BwdParams pk = make_dkdv_params(a);
     const DqParams pq = make_dq_params(a);
     const int units = pk.T * pk.BH + pq.T * pq.BH;
-    const int sms = sm_count();
+    const int sms = device_sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     const int smem = max(BwdCfg<128>::kSmem, DqCfg<128>::kSmem);
     auto kernel = fa_bwd_persist_kernel<128>;

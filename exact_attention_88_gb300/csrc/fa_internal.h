@@ -109,6 +109,10 @@ bool encode_bwd_maps(const BwdArgs& a, CUtensorMap m[4]);
 // it is a __device__ variable), or nullptr on failure.
 int* device_status();
 
+// Streaming multiprocessors of the current device (0 when the query fails),
+// looked up once per device.
+int device_sm_count();
+
 // Launch with programmatic stream serialization: the kernel's CTAs may become
 // resident while the kernel ahead of it on the stream finishes; the kernel
 // waits for that one (pdl_wait) before touching global memory.
