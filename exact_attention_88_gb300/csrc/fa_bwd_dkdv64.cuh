@@ -134,6 +134,22 @@ __device__ __forceinline__ void dkdv64_cta(const CUtensorMap& tmQ, const CUtenso
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const bool keys_live = kt * 128 < kv_limit;  // else every key of the tile is padding
+  if (!keys_live) {
+    // every key of the tile is padding: its dK, dV rows are zero and no MMA
+    // runs, so the CTA writes them and leaves before any set-up (key padding
+    // leaves about a third of the key tiles dead at BERT's lengths)
+    constexpr int kRowChunks = D / 8;  // 16-byte chunks of a row
+    for (int e = tid; e < 2 * 128 * kRowChunks; e += blockDim.x) {
+      const int which = e / (128 * kRowChunks), r = (e / kRowChunks) % 128, c = e % kRowChunks;
+      const int key = kt * 128 + r;
+      if (key < p.N) {
+        __nv_bfloat16* row = which == 0 ? p.dv + row_offset(p.ldv, b, hd, key)
+                                        : p.dk + row_offset(p.ldk, b, hd, key);
+        reinterpret_cast<uint4*>(row)[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    return;
+  }
   if (p.block_mask) build_tile_bitmap(mask_bits, p.block_mask + kt, (size_t)p.T, p.T);
   const QTiles qtiles{p.block_mask ? mask_bits : nullptr, p.T, p.causal ? kt : 0};
   const int iend = keys_live ? p.T : 0;
