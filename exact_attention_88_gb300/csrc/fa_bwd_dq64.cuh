@@ -117,6 +117,11 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
   const int jkv = (kv_limit + 127) / 128;
   if (p.block_mask) build_tile_bitmap(mask_bits, p.block_mask + (size_t)qi * p.T, 1, p.T);
   const KTiles ktiles{p.block_mask ? mask_bits : nullptr, p.causal ? min(jkv, qi + 1) : jkv};
+  // 64-key steps of key tile j: the second is skipped when key padding hides
+  // every key of it (no causal row of a tile the CTA sees loses a whole half).
+  // Every role skips the same steps, and the step barriers count the steps
+  // that run.
+  auto steps_of = [&](int j) { return kv_limit > j * 128 + 64 ? 2 : 1; };
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
@@ -206,15 +211,16 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
       const uint64_t dDO_k = sdesc_sw128(smem_addr(smem + C::kOffDO), 16, 1024);
       const uint32_t sK = smem_addr(smem + C::kOffK), sV = smem_addr(smem + C::kOffV);
       bool ok = true;
-      int u = 0;
+      int u = 0, se = 0;  // key tiles, steps run
       if (role == 0) {
         ok = mbar_wait(&q_full, 0, &abort_flag, p.status, 2100);
         for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
           const int ks = u % C::kKStages;
           ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 2101);
           const uint64_t dK_k = sdesc_sw128(sK + ks * C::kTileBytes, 16, 1024);
-          for (int h = 0; h < 2 && ok; ++h) {
-            const int s = 2 * u + h;
+          const int nh = steps_of(j);
+          for (int h = 0; h < nh && ok; ++h, ++se) {
+            const int s = se;
             if (s > 0) ok = mbar_wait(&s_free, (s - 1) & 1, &abort_flag, p.status, 2102);
             if (!ok) break;
             tc_fence_after();
@@ -233,8 +239,9 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
           const int vs = u % C::kVStages;
           ok = mbar_wait(&v_full[vs], (u / C::kVStages) & 1, &abort_flag, p.status, 2104);
           const uint64_t dV_k = sdesc_sw128(sV + vs * C::kTileBytes, 16, 1024);
-          for (int h = 0; h < 2 && ok; ++h) {
-            const int s = 2 * u + h, x = s & 1;
+          const int nh = steps_of(j);
+          for (int h = 0; h < nh && ok; ++h, ++se) {
+            const int s = se, x = s & 1;
             if (s >= 2) ok = mbar_wait(&dq_done[x], ((s - 2) >> 1) & 1, &abort_flag, p.status, 2105);
             if (!ok) break;
             tc_fence_after();
@@ -255,8 +262,9 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
           const int ks = u % C::kKStages;
           ok = mbar_wait(&k_full[ks], (u / C::kKStages) & 1, &abort_flag, p.status, 2106);
           const uint64_t dK_mn = sdesc_sw128(sK + ks * C::kTileBytes, C::kChunkBytes, 1024);
-          for (int h = 0; h < 2 && ok; ++h) {
-            const int s = 2 * u + h, x = s & 1;
+          const int nh = steps_of(j);
+          for (int h = 0; h < nh && ok; ++h, ++se) {
+            const int s = se, x = s & 1;
             ok = mbar_wait(&ds_ready[x], (s >> 1) & 1, &abort_flag, p.status, 2107);
             if (!ok) break;
             tc_fence_after();
@@ -292,12 +300,13 @@ __device__ __forceinline__ void dq64_cta(const CUtensorMap& tmQ, const CUtensorM
     }
     const float2 c2 = make_float2(p.scale_log2, p.scale_log2), nl22 = make_float2(nl2, nl2);
     const float2 sc2 = make_float2(p.scale, p.scale), nd2 = make_float2(nd, nd);
-    int u = 0;
+    int u = 0, se = 0;  // key tiles, steps run
     bool ok = true;
     for (int j = jfirst; ok && j < ktiles.jend; j = ktiles.next(j + 1), ++u) {
+      const int nh = steps_of(j);
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int s = 2 * u + h, x = s & 1;
+      for (int h = 0; h < nh; ++h, ++se) {
+        const int s = se, x = s & 1;
         const uint32_t tP = tmem + C::kColDP + 64 * x + lane_off + col0;
         // keys [key0, key0 + 32) of this warpgroup; visible: key < kv_limit and,
         // causal, key <= q
