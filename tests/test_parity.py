@@ -124,6 +124,22 @@ def test_unseen_key_tiles_and_all_padding(fa, d):
         assert torch.all(dq[0] == 0) and torch.all(dk[0] == 0) and torch.all(dv[0] == 0)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_lengths_at_step_boundaries(fa, d, causal):
+    """Key lengths at and beside the 64-key step and 128-key tile boundaries:
+    the d = 64 dQ CTA skips a step whose 64 keys all lie past the length (64,
+    192: the last tile's second half empty; 65, 129: one key in it), and the
+    dK/dV CTAs of tiles past the length write zero rows and leave before
+    set-up (1: three of the four tiles; 128, 256: whole tiles)."""
+    N = 512
+    kv = np.array([64, 65, 127, 128, 129, 192, 1, 256], np.int32)
+    case = random_case(len(kv), 2, N, d, seed=61 + d + causal, kv_len=kv)
+    o, lse, (dq, dk, dv) = check_full(fa, case, len(kv), 2, N, d, causal, "bf16")
+    for bi, L in enumerate(kv):
+        assert torch.all(dk[bi, :, L:] == 0) and torch.all(dv[bi, :, L:] == 0)
+
+
 @pytest.mark.parametrize("name", ["tiny_fp32", "tiny_fp32_causal"])
 def test_workload_tiny_fp32(fa, name):
     w = WORKLOADS[name]
