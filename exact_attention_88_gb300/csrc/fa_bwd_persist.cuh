@@ -8,9 +8,10 @@
 // The arithmetic is that of the dQ CTA (fa_bwd_dq.cuh; "FlashAttention: Fast
 // and Memory-Efficient Exact Attention with IO-Awareness", summary page, "Key
 // ideas: recomputation in the backward pass"), with the same TMEM columns,
-// rings and roles, and dQ is bit-identical to its: a unit runs the same MMAs
-// in the same order.  The combined backward kernel uses it for the calls
-// without a block mask, key padding, dropout or a bias at d = 128.
+// rings and roles, and dQ is bit-identical to the one-per-unit CTA's: a unit
+// runs the same MMAs in the same order.  The combined backward kernel uses
+// it for the calls without a block mask, key padding, dropout or a bias at
+// d = 128.
 //
 // Units: the combined kernel's dK/dV CTAs take units [0, n0); [n0, n) are the
 // dQ query tiles in their grid order (heaviest first).  The persistent CTA x
