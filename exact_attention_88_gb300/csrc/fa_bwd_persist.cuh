@@ -119,6 +119,8 @@ __device__ __forceinline__ void dq_persist(const CUtensorMap& tmQ, const CUtenso
                                            const DqParams& p, uint32_t tmem, int first, int n0,
                                            int n, int* counter) {
   using C = DqCfg<D>;
+  static_assert(kUnitConsumers == 3 + C::kMathWarps,
+                "every MMA issuer and every math warp takes each unit from the ring");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
