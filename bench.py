@@ -35,17 +35,22 @@ from workloads import WORKLOADS, generate, flops, sha256  # noqa: E402
 
 METRIC = "attention fwd+bwd TFLOP/s (bf16, causal, 1 GB300) and % of dense bf16 peak"
 DEFAULT_WORKLOAD = "long_causal_d128"
-# DRAM bytes (read + write) of one fa_bwd_dkdv launch on the default workload,
-# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# current version of that kernel; set to None whenever the kernel changes
-# until it is captured again.
-DKDV_DRAM_BYTES = {"long_causal_d128": 380701952 + 103244032}
+# DRAM bytes (read + write) of one launch on the default workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the current
+# version of each kernel: the combined backward kernel that fa_bwd launches
+# after its preprocess, and the standalone dK/dV kernel; set to None whenever
+# a kernel changes until it is captured again.
+DRAM_BYTES = {"long_causal_d128": {"bwd_combined": 808603392 + 189961216,
+                                   "bwd_dkdv": 380701952 + 103244032}}
 # Tensor-pipe activity of each kernel on the default workload: the fraction of
 # elapsed cycles the tensor pipe was active (sm__pipe_tensor_cycles_active,
 # pct_of_peak_sustained_elapsed) in one-kernel ncu captures of the current
 # kernels; set to None whenever a kernel changes until it is captured again.
 TENSOR_PIPE_ACTIVE = {"long_causal_d128": {"fwd": 0.509, "bwd_preprocess": 0.0,
-                                           "bwd_dkdv": 0.607, "bwd_dq": 0.696}}
+                                           "bwd_combined": 0.654, "bwd_dkdv": 0.607,
+                                           "bwd_dq": 0.696}}
+# the kernels a timed step launches (the work-order kernel aside)
+STEP_KERNELS = ("fwd", "bwd_preprocess", "bwd_combined")
 
 
 def measured_peaks():
@@ -317,13 +322,15 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
 
     kernels = (["mask_order"] if order is not None else []) + [
-        "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq"]
+        "fwd", "bwd_preprocess", "bwd_dkdv", "bwd_dq", "bwd"]
     ev = {n: [] for n in kernels}
 
     # A timed step is the public calls: fa_fwd_ex, then fa_bwd_ex (the D
     # preprocess, then dK/dV and dQ in one launch whose dQ CTAs fill the SMs the
     # last dK/dV CTAs leave idle).  The per-kernel pass times the same kernels
-    # through the one-step calls, each between CUDA events on the stream.
+    # through the one-step calls, each between CUDA events on the stream, and
+    # fa_bwd_ex as the step runs it: its time less the preprocess launch's is
+    # the combined kernel's.
     def step(record):
         def mark(name, fn):
             if record:
@@ -348,6 +355,8 @@ def run_gpu(args, rank, world, local_rank):
                                                    w.causal, mask, opt, stream))
         mark("bwd_dq", lambda: fa.fa_bwd_dq_ex(q, k, v, do, lse, D, dq, B, H, N, d, scale,
                                                w.causal, mask, opt, stream))
+        mark("bwd", lambda: fa.fa_bwd_ex(q, k, v, o, do, lse, dq, dk, dv, ws, ws_bytes, B, H, N,
+                                         d, scale, w.causal, mask, opt, stream))
 
     dist = None
     if world > 1:
@@ -391,6 +400,7 @@ def run_gpu(args, rank, world, local_rank):
     if code != 0:
         raise RuntimeError("device status %d at site %d in the timed region" % (code, site))
     per_kernel = {n: statistics.mean(a.elapsed_time(b) for a, b in ev[n]) for n in kernels}
+    per_kernel["bwd_combined"] = max(per_kernel["bwd"] - per_kernel["bwd_preprocess"], 1e-6)
 
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / args.steps
@@ -404,6 +414,13 @@ def run_gpu(args, rank, world, local_rank):
     # count); dQ kernel S, dP, dQ (only dQ algorithmic, S and dP recomputed again)
     dkdv_flops = 2.0 * fwd_flops
     dq_flops = 1.5 * fwd_flops
+    # the combined kernel does the backward's algorithmic work (2.5 x fwd) and
+    # executes dK/dV's and dQ's GEMMs (3.5 x fwd)
+    bwd_flops = 2.5 * fwd_flops
+    bwd_executed = dkdv_flops + dq_flops
+    bwd_achieved = bwd_flops / (per_kernel["bwd_combined"] * 1e-3) / 1e12
+    bwd_exec_achieved = bwd_executed / (per_kernel["bwd_combined"] * 1e-3) / 1e12
+    dram = DRAM_BYTES.get(w.name, {})
     achieved = dkdv_flops / (per_kernel["bwd_dkdv"] * 1e-3) / 1e12
     dq_achieved = dq_flops / (per_kernel["bwd_dq"] * 1e-3) / 1e12
     fwd_achieved = fwd_flops / (per_kernel["fwd"] * 1e-3) / 1e12
@@ -431,16 +448,30 @@ def run_gpu(args, rank, world, local_rank):
         "pct_of_peak": round(100.0 * (value / world) / peak, 2),
         "inputs_sha256": inputs_sha256,
         "kernels_ms": {n: round(t, 4) for n, t in per_kernel.items()},
+        # the step's dominant kernel: fa_bwd's combined dK/dV + dQ launch
         "roofline": {
-            "kernel": "fa_bwd_dkdv (S^T, dP^T, dV, dK on tcgen05)",
+            "kernel": "fa_bwd combined kernel (dK/dV CTAs, then dQ CTAs, on tcgen05)",
             "bound": "tensor",
-            "achieved": round(achieved, 2),
+            "achieved": round(bwd_achieved, 2),
             "peak": peak,
             "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4),
+            "frac": round(bwd_achieved / peak, 4),
             "peak_source": "bf16 burst, %s (MEASURED_PEAKS.json)" % peak_kind,
-            "traffic": DKDV_DRAM_BYTES.get(w.name),
+            "traffic": dram.get("bwd_combined"),
             "traffic_unit": "bytes per launch (ncu capture)",
+            "flops_per_launch": bwd_flops,
+            "duration_ms": round(per_kernel["bwd_combined"], 4),
+            "duration_source": "CUDA events around fa_bwd_ex (preprocess + combined kernel) "
+                               "less those around the preprocess launch alone",
+            "executed_flops_per_launch": bwd_executed,
+            "executed_achieved": round(bwd_exec_achieved, 2),
+            "executed_frac": round(bwd_exec_achieved / peak, 4),
+        },
+        "dkdv_roofline": {
+            "kernel": "fa_bwd_dkdv (S^T, dP^T, dV, dK on tcgen05; the standalone call)",
+            "achieved": round(achieved, 2),
+            "frac": round(achieved / peak, 4),
+            "traffic": dram.get("bwd_dkdv"),
             "flops_per_launch": dkdv_flops,
         },
         "fwd_roofline": {"kernel": "fa_fwd", "achieved": round(fwd_achieved, 2),
@@ -477,16 +508,16 @@ def tensor_pipe_share(workload, per_kernel_ms, step_flops, fwd_flops):
     of which S and dP are a second recomputation) = 4.5 x fwd_flops, while the
     metric counts 3.5 x fwd_flops."""
     act = TENSOR_PIPE_ACTIVE.get(workload)
-    if not act or any(v is None for v in act.values()):
+    if not act or any(act.get(k) is None for k in STEP_KERNELS):
         return None
-    total = sum(per_kernel_ms.values())
-    busy = sum(act[k] * per_kernel_ms[k] for k in act) / total
+    total = sum(per_kernel_ms[k] for k in STEP_KERNELS)
+    busy = sum(act[k] * per_kernel_ms[k] for k in STEP_KERNELS) / total
     executed = fwd_flops + 2.0 * fwd_flops + 1.5 * fwd_flops
     return {"active_time_weighted": round(busy, 4),
             "executed_tflop": round(executed / 1e12, 4),
             "algorithmic_tflop": round(step_flops / 1e12, 4),
             "algorithmic_active": round(busy * step_flops / executed, 4),
-            "per_kernel_active": act,
+            "per_kernel_active": {k: act[k] for k in STEP_KERNELS},
             "source": "one-kernel ncu --set full captures (sm__pipe_tensor_cycles_active, "
                       "% of elapsed cycles), weighted by this run's per-kernel times"}
 
