@@ -57,6 +57,10 @@ struct DqCfg {
   static constexpr int kMathWarps = 16;
   static constexpr int kThreads = kMathWarps * 32 + 128;  // + producer, three MMA issuers
   static constexpr int kDSlice = D / 4;  // d columns per warpgroup in the read-out
+  // V stage u % kVStages is also dP buffer u & 1 (two buffers of 128 columns
+  // between kColDP and kColDQ)
+  static_assert(kVStages == 2 && kColDP + 2 * 128 == kColDQ && kColDQ + D <= kTmemCols,
+                "dP is double-buffered by the V stage");
 };
 
 struct DqParams {
