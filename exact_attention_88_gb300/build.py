@@ -27,6 +27,7 @@ SOURCES = [
     "fa_api.cu",
     "fa_fwd_sm103.cu",
     "fa_fwd64_sm103.cu",
+    "fa_fwd128s_sm103.cu",
     "fa_bwd_sm103.cu",
     "fa_bwd_dkdv64_sm103.cu",
     "fa_bwd_dq64_sm103.cu",

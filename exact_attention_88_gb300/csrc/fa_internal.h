@@ -135,6 +135,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_fwd64_bf16(const FwdArgs& a, cudaStream_t s);  // d = 64, plain
+cudaError_t launch_fwd128s_bf16(const FwdArgs& a, cudaStream_t s);  // d = 128, plain
 cudaError_t launch_bwd_preprocess(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_bf16(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_dkdv64_bf16(const BwdArgs& a, cudaStream_t s);  // d = 64, plain
