@@ -78,16 +78,14 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
                                                 bool first, float& m, float& l, uint64_t* pv_prev,
                                                 uint32_t pv_parity, volatile int* abort_flag,
                                                 int* status, int site) {
-  float tmax;
-  {
-    uint32_t r[32];
-    FA_TMEM_LD32_SYNC(tS, r);
-    if (lim < 32) mask32(r, lim);
-    tmax = max32(r);
-    FA_TMEM_LD32_SYNC(tS + 32, r);
-    if (lim < 64) mask32(r, lim - 32);
-    tmax = fmaxf(tmax, max32(r)) * scale_log2;
+  // the half-row's 64 scores, loaded once (one wait) for both passes
+  uint32_t r[64];
+  FA_TMEM_LD64_SYNC(tS, r);
+  if (lim < 64) {
+    mask32(r, lim);
+    mask32(r + 32, lim - 32);
   }
+  const float tmax = fmaxf(max32(r), max32(r + 32)) * scale_log2;
   const float m_new = fmaxf(m, tmax);
   const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
   float alpha = 1.f;
@@ -112,23 +110,16 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
   float2 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
-#pragma unroll 1
-  for (int c = 0; c < 2; ++c) {
-    uint32_t r[32];
-    FA_TMEM_LD32_SYNC(tS + 32 * c, r);
-    if (lim < 64) mask32(r, lim - 32 * c);
-    uint32_t pk[16];
+  uint32_t pk[32];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
-      const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-      acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-      pk[e >> 1] = pack_bf16(pv.x, pv.y);
-    }
-    // packed P~ of keys [32c, 32c + 32) over the half's columns [16c, 16c + 16),
-    // which this thread has already read
-    FA_TMEM_ST16(tS + 16 * c, pk);
+  for (int e = 0; e < 64; e += 2) {
+    const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
+    const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+    acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+    pk[e >> 1] = pack_bf16(pv.x, pv.y);
   }
+  // packed P~ of the 64 keys over the half's first 32 columns, already read
+  FA_TMEM_ST32(tS, pk);
   const float2 st = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
   l = l * alpha + (st.x + st.y);
   tmem_wait_st();
