@@ -24,8 +24,10 @@
 // Roles (384 threads): warps 0-3 softmax of keys [0,64), warps 4-7 of keys
 // [64,128) (thread = query row), warp 8 TMA producer (Q once; a K ring of 3
 // and a V ring of 2, each K loaded one key tile ahead of its V), warp 9 issues
-// S, warps 10 and 11 issue P~_0 V and P~_1 V (one thread each).
-// The barriers signalled per key tile (s_full, p_full, pv_done) are kept per
+// S, warps 10 and 11 issue P~_0 V and P~_1 V (one thread each): the MMAs of a
+// half's first 32 keys as soon as the softmax has written their P~ (p_half),
+// the other two once the whole half is written (p_full).
+// The barriers signalled per key tile (s_full, p_half, p_full, pv_done) are kept per
 // score buffer: each has one phase per use of its buffer, and a buffer's next
 // use needs its waiters' own progress first, so no waiter can fall two phases
 // behind (a K load that arrives late cannot let a per-tile phase run ahead).
@@ -77,7 +79,7 @@ struct Fwd128sParams {
 __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int lim, float scale_log2,
                                                 bool first, float& m, float& l, uint64_t* pv_prev,
                                                 uint32_t pv_parity, volatile int* abort_flag,
-                                                int* status, int site) {
+                                                int* status, int site, uint64_t* p_half) {
   // the half-row's 64 scores, loaded once (one wait) for both passes
   uint32_t r[64];
   FA_TMEM_LD64_SYNC(tS, r);
@@ -110,16 +112,26 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
   float2 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
-  uint32_t pk[32];
+  // packed P~ of keys [32c, 32c + 32) over the half's columns [16c, 16c + 16),
+  // already read; the first 32 keys are signalled as soon as they are written
 #pragma unroll
-  for (int e = 0; e < 64; e += 2) {
-    const float2 xx = fma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), c2, nm2);
-    const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-    acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
-    pk[e >> 1] = pack_bf16(pv.x, pv.y);
+  for (int c = 0; c < 2; ++c) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int i = 32 * c + e;
+      const float2 xx = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+      const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+      acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+      pk[e >> 1] = pack_bf16(pv.x, pv.y);
+    }
+    FA_TMEM_ST16(tS + 16 * c, pk);
+    if (c == 0) {
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(p_half);
+    }
   }
-  // packed P~ of the 64 keys over the half's first 32 columns, already read
-  FA_TMEM_ST32(tS, pk);
   const float2 st = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
   l = l * alpha + (st.x + st.y);
   tmem_wait_st();
@@ -134,10 +146,11 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t q_full, drain[3];
-  // per score buffer x: s_full (S in it), and per half h: p_full (P~_h written,
-  // one arrival per warp of warpgroup h), pv_done (P~_h V done: O_h is current
-  // and the half's columns of the buffer are free)
-  __shared__ uint64_t s_full[2], p_full[2][2], pv_done[2][2];
+  // per score buffer x: s_full (S in it), and per half h: p_half / p_full (P~_h
+  // of the first 32 keys / of all 64 written, one arrival per warp of warpgroup
+  // h), pv_done (P~_h V done: O_h is current and the half's columns of the
+  // buffer are free)
+  __shared__ uint64_t s_full[2], p_half[2][2], p_full[2][2], pv_done[2][2];
   __shared__ uint64_t k_full[C::kKStages], k_empty[C::kKStages];
   __shared__ uint64_t v_full[C::kVStages], v_empty[C::kVStages];
   __shared__ uint32_t tmem_slot;
@@ -163,6 +176,7 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
       for (int h = 0; h < 2; ++h) {
+        mbar_init(&p_half[x][h], 4);
         mbar_init(&p_full[x][h], 4);
         mbar_init(&pv_done[x][h], 1);
       }
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
       for (int u = 0; ok && u < nt; ++u) {
         const int st = u % C::kVStages, x = u & 1;
         ok = mbar_wait(&v_full[st], (u / C::kVStages) & 1, &abort_flag, p.status, 2415);
-        if (ok) ok = mbar_wait(&p_full[x][h], (u >> 1) & 1, &abort_flag, p.status, 2416 + h);
+        if (ok) ok = mbar_wait(&p_half[x][h], (u >> 1) & 1, &abort_flag, p.status, 2418 + h);
         if (!ok) break;
         tc_fence_after();
         // O_h += P~_h V rows [64h, 64h + 64): P~ of 16 keys per 8 packed
@@ -277,9 +291,15 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
         const uint64_t dV = sdesc_sw128(sV + st * C::kTileBytes, C::kChunkBytes, 1024);
         const uint32_t tP = tmem + C::kColS + 128 * x + 64 * h;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+        for (int kk = 0; kk < 2; ++kk)
           mma_ts(tO, tP + 8 * kk, dV + (4 * h + kk) * (2048 >> 4), idesc_pv,
                  (u > 0 || kk > 0) ? 1u : 0u);
+        ok = mbar_wait(&p_full[x][h], (u >> 1) & 1, &abort_flag, p.status, 2416 + h);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 2; kk < 4; ++kk)
+          mma_ts(tO, tP + 8 * kk, dV + (4 * h + kk) * (2048 >> 4), idesc_pv, 1u);
         mma_commit(&pv_done[x][h]);
         mma_commit(&v_empty[st]);
       }
@@ -307,7 +327,7 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
       // the previous key tile's P~_h V: buffer x ^ 1, that buffer's use (n - 1) / 2
       ok = softmax_half128(tmem + C::kColS + 128 * x + 64 * h + lane_off, tO, lim, p.scale_log2,
                            n == 0, m, l, &pv_done[x ^ 1][h], ((n - 1) >> 1) & 1, &abort_flag,
-                           p.status, 2423 + h);
+                           p.status, 2423 + h, &p_half[x][h]);
       if (!ok) break;
       tc_fence_before();
       mbar_arrive_warp(&p_full[x][h]);
