@@ -31,7 +31,11 @@
 // score buffer: each has one phase per use of its buffer, and a buffer's next
 // use needs its waiters' own progress first, so no waiter can fall two phases
 // behind (a K load that arrives late cannot let a per-tile phase run ahead).
-// This is the kernel of d = 128 calls without dropout, a bias or a block mask.
+// This is the kernel of d = 128 calls without a block mask.  The kExtra variant
+// adds dropout (a row's 64 keep bits of the half, drawn while the warpgroup waits
+// for the tile's scores; dropped entries of P~ are zeroed in the packed P~ but
+// counted in l, and O is scaled by 1 / (1 - p) at the end) and an additive bias
+// (added to the scaled scores before the maximum).
 #include "fa_common.cuh"
 #include "fa_internal.h"
 
@@ -68,6 +72,9 @@ struct Fwd128sParams {
   float scale_log2;
   int causal;
   int* status;
+  DropParams drop;
+  const float* bias;  // additive score bias or nullptr
+  Layout lb;
 };
 
 // Softmax of this warpgroup's 64 keys of one key tile for this thread's row:
@@ -75,11 +82,31 @@ struct Fwd128sParams {
 // tO: the half's O columns (lane offset included).  O_h is rescaled only after
 // the previous key tile's P~_h V has completed (pv_prev, pv_parity): the S of
 // this tile may have been issued before it.  Returns false when that wait
-// gave up.
+// gave up.  kExtra: kbits holds the keep bits of the half's keys [0, 32) and
+// [32, 64) (all set without dropout), brow this row's bias (nullptr past the
+// end; bias_on warp-uniform), key0 the half's first key, n_keys the keys of a
+// bias row.
+// Keep bits of keys key0 + c, c = 0..63 (word c / 32, bit c % 32), of query row
+// i: the bits keep_bits_of_row gives for key0 and key0 + 32, with all eight
+// Philox calls in flight at once.
+__device__ __forceinline__ void keep_bits64_of_row(const DropParams& d, uint32_t bh, int i, int key0,
+                                                   uint32_t* out) {
+  uint4 w[8];
+#pragma unroll
+  for (int g = 0; g < 8; ++g)
+    w[g] = philox4x32_10((uint32_t)(key0 >> 3) + g, (uint32_t)i, bh, d.offset, d.k0, d.k1);
+  out[0] = out[1] = 0u;
+#pragma unroll
+  for (int g = 0; g < 8; ++g) out[g >> 2] |= keep_bits8(w[g], d.t) << (8 * (g & 3));
+}
+
+template <bool kExtra>
 __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int lim, float scale_log2,
                                                 bool first, float& m, float& l, uint64_t* pv_prev,
                                                 uint32_t pv_parity, volatile int* abort_flag,
-                                                int* status, int site, uint64_t* p_half) {
+                                                int* status, int site, uint64_t* p_half,
+                                                const uint32_t* kbits, bool bias_on,
+                                                const float* brow, int key0, int n_keys) {
   // the half-row's 64 scores, loaded once (one wait) for both passes
   uint32_t r[64];
   FA_TMEM_LD64_SYNC(tS, r);
@@ -87,7 +114,16 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
     mask32(r, lim);
     mask32(r + 32, lim - 32);
   }
-  const float tmax = fmaxf(max32(r), max32(r + 32)) * scale_log2;
+  float exp_scale = scale_log2;  // multiplies what the exponent pass reads from r
+  if (kExtra && bias_on) {
+    // biased scores in log2 units: S scale log2(e) + bias log2(e)
+    float bv[64];
+    load_bias_row<64>(brow, key0, n_keys, bv);
+#pragma unroll
+    for (int e = 0; e < 64; ++e) r[e] = __float_as_uint(fmaf(__uint_as_float(r[e]), scale_log2, bv[e]));
+    exp_scale = 1.f;
+  }
+  const float tmax = fmaxf(max32(r), max32(r + 32)) * exp_scale;
   const float m_new = fmaxf(m, tmax);
   const bool grow = m_new > m + kRescaleThreshold;  // true when m = -inf, m_new finite
   float alpha = 1.f;
@@ -108,7 +144,7 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
     }
   }
   const float nm = (m == -INFINITY) ? 0.f : -m;
-  const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(nm, nm);
+  const float2 c2 = make_float2(exp_scale, exp_scale), nm2 = make_float2(nm, nm);
   float2 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
@@ -121,8 +157,12 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
     for (int e = 0; e < 32; e += 2) {
       const int i = 32 * c + e;
       const float2 xx = fma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
-      const float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
-      acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);
+      float2 pv = make_float2(ex2(xx.x), ex2(xx.y));
+      acc[(e >> 1) & 3] = add2(acc[(e >> 1) & 3], pv);  // l sums the undropped P~
+      if constexpr (kExtra) {  // dropout (all bits set without it)
+        if (!((kbits[c] >> e) & 1u)) pv.x = 0.f;
+        if (!((kbits[c] >> (e + 1)) & 1u)) pv.y = 0.f;
+      }
       pk[e >> 1] = pack_bf16(pv.x, pv.y);
     }
     FA_TMEM_ST16(tS + 16 * c, pk);
@@ -138,6 +178,7 @@ __device__ __forceinline__ bool softmax_half128(uint32_t tS, uint32_t tO, int li
   return true;
 }
 
+template <bool kExtra>
 __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
     fa_fwd128s_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const Fwd128sParams p) {
@@ -315,8 +356,16 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
     const uint32_t tO = tmem + C::kColO + 128 * h + lane_off;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
+    // additive bias: this row's [N] bias (nullptr past the end of the sequence)
+    const bool bias_on = kExtra && p.bias != nullptr;
+    const float* brow = (bias_on && row < p.N) ? p.bias + row_offset(p.lb, b, hd, row) : nullptr;
     for (int n = 0; n < nt; ++n) {
       const int x = n & 1;
+      // dropout: this row's keep bits of the half, drawn before the wait for S
+      uint32_t kbits[2] = {~0u, ~0u};
+      if constexpr (kExtra) {
+        if (p.drop.t) keep_bits64_of_row(p.drop, (uint32_t)bh, row, n * 128 + 64 * h, kbits);
+      }
       ok = mbar_wait_warp(&s_full[x], (n >> 1) & 1, &abort_flag, p.status, 2421 + h);
       if (!ok) break;
       tc_fence_after();
@@ -325,9 +374,10 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
       int lim = kv_limit - key0;
       if (p.causal) lim = min(lim, row - key0 + 1);
       // the previous key tile's P~_h V: buffer x ^ 1, that buffer's use (n - 1) / 2
-      ok = softmax_half128(tmem + C::kColS + 128 * x + 64 * h + lane_off, tO, lim, p.scale_log2,
-                           n == 0, m, l, &pv_done[x ^ 1][h], ((n - 1) >> 1) & 1, &abort_flag,
-                           p.status, 2423 + h, &p_half[x][h]);
+      ok = softmax_half128<kExtra>(tmem + C::kColS + 128 * x + 64 * h + lane_off, tO, lim,
+                                   p.scale_log2, n == 0, m, l, &pv_done[x ^ 1][h],
+                                   ((n - 1) >> 1) & 1, &abort_flag, p.status, 2423 + h,
+                                   &p_half[x][h], kbits, bias_on, brow, key0, p.N);
       if (!ok) break;
       tc_fence_before();
       mbar_arrive_warp(&p_full[x][h]);
@@ -350,7 +400,8 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
       const float a1 = (m1 == -INFINITY) ? 0.f : ex2(m1 - mm);
       const float lt = s_l[0][tq] * a0 + s_l[1][tq] * a1;
       const bool empty_row = !(lt > 0.f);
-      const float inv = empty_row ? 0.f : 1.f / lt;
+      // dropout: the kept entries of P are scaled by 1 / (1 - p)
+      const float inv = empty_row ? 0.f : (kExtra ? p.drop.rp : 1.f) / lt;
       const float w0 = a0 * inv, w1 = a1 * inv;
       // warpgroup h writes d columns [64h, 64h + 64) of the row
 #pragma unroll 1
@@ -417,11 +468,13 @@ cudaError_t launch_fwd128s_bf16(const FwdArgs& a, cudaStream_t s) {
   p.scale_log2 = a.scale * kLog2e;
   p.causal = a.causal;
   p.status = a.status;
-  cudaError_t e =
-      cudaFuncSetAttribute(fa_fwd128s_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  p.drop = a.drop;
+  p.bias = a.bias;
+  p.lb = a.lb;
+  auto kernel = (a.drop.t || a.bias) ? fa_fwd128s_kernel<true> : fa_fwd128s_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(fa_fwd128s_kernel, dim3(p.T * BH), dim3(C::kThreads), C::kSmem, s, mq, mk, mv,
-                    p);
+  return launch_pdl(kernel, dim3(p.T * BH), dim3(C::kThreads), C::kSmem, s, mq, mk, mv, p);
 }
 
 }  // namespace fa

@@ -8,7 +8,8 @@
 // Online Softmax to FlashAttention", "Algorithm FlashAttention (Tiling)").  The
 // division by l is deferred to the end, which is the same quantity.
 //
-// d = 128: one CTA owns two 128-row query tiles (A and B) of one (batch,
+// d = 128 with a block mask (calls without one take fa_fwd128s_sm103.cu, one
+// query tile per CTA with two score buffers): one CTA owns two 128-row query tiles (A and B) of one (batch,
 // head) and streams the key/value tiles through a shared ring.  The two tiles
 // alternate on the tensor core: while one tile's softmax runs on its
 // warpgroup, the other tile's S = Q K^T or O += P V is computed, so the tensor
@@ -564,8 +565,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
   if (a.d == 64 && !a.drop.t && !a.bias) return launch_fwd64_bf16(a, s);
-  if (a.d == 128 && !a.drop.t && !a.bias && a.mask_kind != FA_MASK_BLOCK_SPARSE)
-    return launch_fwd128s_bf16(a, s);
+  if (a.d == 128 && a.mask_kind != FA_MASK_BLOCK_SPARSE) return launch_fwd128s_bf16(a, s);
   return a.d == 64 ? launch_fwd_d<64, 1>(a, s) : launch_fwd_d<128, 2>(a, s);
 }
 
