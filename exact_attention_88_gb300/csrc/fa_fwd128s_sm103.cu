@@ -31,7 +31,10 @@
 // score buffer: each has one phase per use of its buffer, and a buffer's next
 // use needs its waiters' own progress first, so no waiter can fall two phases
 // behind (a K load that arrives late cannot let a per-tile phase run ahead).
-// This is the kernel of d = 128 calls without a block mask.  The kExtra variant
+// With a block mask, a CTA walks only the key tiles its query tile sees (the
+// mask row as a shared-memory bitmap), and a block-sparse work order may say
+// which query tile each CTA takes.  This is the kernel of every d = 128
+// call.  The kExtra variant
 // adds dropout (a row's 64 keep bits of the half, drawn while the warpgroup waits
 // for the tile's scores; dropped entries of P~ are zeroed in the packed P~ but
 // counted in l, and O is scaled by 1 / (1 - p) at the end) and an additive bias
@@ -75,6 +78,25 @@ struct Fwd128sParams {
   DropParams drop;
   const float* bias;  // additive score bias or nullptr
   Layout lb;
+  const uint8_t* block_mask;  // T x T tile mask or nullptr
+  const int32_t* order;       // block-sparse work order (query tiles) or nullptr
+};
+
+// Key tiles j < jend that a query tile sees: all of them, or those set in
+// its block-mask row (a shared-memory bitmap).
+struct KTiles {
+  const uint32_t* bits;
+  int jend;
+  __device__ int next(int j) const { return bits ? next_tile_bit(bits, j, jend) : j; }
+  __device__ int count() const {
+    if (!bits) return jend;
+    int c = 0;
+    for (int w = 0; 32 * w < jend; ++w) {
+      const int rest = jend - 32 * w;
+      c += __popc(rest < 32 ? bits[w] & ((1u << rest) - 1u) : bits[w]);
+    }
+    return c;
+  }
 };
 
 // Softmax of this warpgroup's 64 keys of one key tile for this thread's row:
@@ -197,19 +219,22 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   __shared__ float s_m[2][128], s_l[2][128];  // each half's final statistics, by row
+  __shared__ uint32_t mask_bits[kMaskBitmapWords];  // block-mask row qi
 
   pdl_wait();  // the kernel ahead on the stream is done (it may write our inputs)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // causal: the last query tiles see the most keys: first
+  // causal: the last query tiles see the most keys: first; a block-sparse work
+  // order lists the query tiles by their visible key tiles
   int order, bh;
   grid_order(blockIdx.x, p.BH, p.T, p.group, &order, &bh);
-  const int qi = p.T - 1 - order;
+  const int qi = ordered_tile(p.order, order, p.T, p.T - 1 - order);
   const int b = bh / p.H;
   const int hd = bh - b * p.H;
   int kv_limit = p.N;
   if (p.kv_len) kv_limit = max(0, min(p.kv_len[b], p.N));
   const int jkv = (kv_limit + 127) / 128;
-  const int nt = p.causal ? min(jkv, qi + 1) : jkv;  // key tiles [0, nt)
+  if (p.block_mask) build_tile_bitmap(mask_bits, p.block_mask + (size_t)qi * p.T, 1, p.T);
+  const KTiles tiles{p.block_mask ? mask_bits : nullptr, p.causal ? min(jkv, qi + 1) : jkv};
 
   if (tid == 0) {
     mbar_init(&q_full, 1);
@@ -239,6 +264,9 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   pdl_launch_dependents();  // TMEM held: the next kernel may become resident
+  // visible key tiles, counted after the barrier (the bitmap is complete); the
+  // u-th of them is key tile tiles.next(...) walked from 0
+  const int nt = tiles.count();
 
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -250,32 +278,37 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
       for (int c = 0; c < 2; ++c)
         tma_load_4d(&tmQ, &q_full, smem + C::kOffQ + c * C::kChunkBytes, c * 64, qi * 128, hd, b);
       int kcount[C::kKStages] = {}, vcount[C::kVStages] = {};
-      auto load_k = [&](int u) {
+      auto load_k = [&](int u, int j) {
         const int st = u % C::kKStages;
         if (!mbar_wait(&k_empty[st], ((u / C::kKStages) & 1) ^ 1, &abort_flag, p.status, 2401))
           return false;
         mbar_expect_tx(&k_full[st], C::kTileBytes);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(&tmK, &k_full[st], smem + C::kOffK + st * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, u * 128, hd, b);
+                      c * 64, j * 128, hd, b);
         ++kcount[st];
         return true;
       };
-      auto load_v = [&](int u) {
+      auto load_v = [&](int u, int j) {
         const int st = u % C::kVStages;
         if (!mbar_wait(&v_empty[st], ((u / C::kVStages) & 1) ^ 1, &abort_flag, p.status, 2402))
           return false;
         mbar_expect_tx(&v_full[st], C::kTileBytes);
         for (int c = 0; c < 2; ++c)
           tma_load_4d(&tmV, &v_full[st], smem + C::kOffV + st * C::kTileBytes + c * C::kChunkBytes,
-                      c * 64, u * 128, hd, b);
+                      c * 64, j * 128, hd, b);
         ++vcount[st];
         return true;
       };
-      bool ok = nt == 0 || load_k(0);
+      int jk = tiles.next(0), jv = jk;  // key tiles of the next K and V loads
+      bool ok = nt == 0 || load_k(0, jk);
       for (int u = 0; ok && u < nt; ++u) {
-        if (u + 1 < nt) ok = load_k(u + 1);
-        if (ok) ok = load_v(u);
+        if (u + 1 < nt) {
+          jk = tiles.next(jk + 1);
+          ok = load_k(u + 1, jk);
+        }
+        if (ok) ok = load_v(u, jv);
+        jv = tiles.next(jv + 1);
       }
       // every issued copy must have landed before the CTA may exit
       mbar_drain(&q_full, 0);
@@ -359,18 +392,19 @@ __global__ void __launch_bounds__(Fwd128sCfg::kThreads, 1)
     // additive bias: this row's [N] bias (nullptr past the end of the sequence)
     const bool bias_on = kExtra && p.bias != nullptr;
     const float* brow = (bias_on && row < p.N) ? p.bias + row_offset(p.lb, b, hd, row) : nullptr;
-    for (int n = 0; n < nt; ++n) {
+    int j = tiles.next(0);
+    for (int n = 0; n < nt; ++n, j = tiles.next(j + 1)) {
       const int x = n & 1;
       // dropout: this row's keep bits of the half, drawn before the wait for S
       uint32_t kbits[2] = {~0u, ~0u};
       if constexpr (kExtra) {
-        if (p.drop.t) keep_bits64_of_row(p.drop, (uint32_t)bh, row, n * 128 + 64 * h, kbits);
+        if (p.drop.t) keep_bits64_of_row(p.drop, (uint32_t)bh, row, j * 128 + 64 * h, kbits);
       }
       ok = mbar_wait_warp(&s_full[x], (n >> 1) & 1, &abort_flag, p.status, 2421 + h);
       if (!ok) break;
       tc_fence_after();
       // keys [key0, key0 + lim) of the half are visible from this row
-      const int key0 = n * 128 + 64 * h;
+      const int key0 = j * 128 + 64 * h;
       int lim = kv_limit - key0;
       if (p.causal) lim = min(lim, row - key0 + 1);
       // the previous key tile's P~_h V: buffer x ^ 1, that buffer's use (n - 1) / 2
@@ -471,6 +505,8 @@ cudaError_t launch_fwd128s_bf16(const FwdArgs& a, cudaStream_t s) {
   p.drop = a.drop;
   p.bias = a.bias;
   p.lb = a.lb;
+  p.block_mask = a.mask_kind == FA_MASK_BLOCK_SPARSE ? a.block_mask : nullptr;
+  p.order = p.block_mask ? a.tile_order : nullptr;  // query tiles at [0, T)
   auto kernel = (a.drop.t || a.bias) ? fa_fwd128s_kernel<true> : fa_fwd128s_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;

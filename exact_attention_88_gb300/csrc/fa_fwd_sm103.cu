@@ -565,7 +565,7 @@ cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t s) {
 
 cudaError_t launch_fwd_bf16(const FwdArgs& a, cudaStream_t s) {
   if (a.d == 64 && !a.drop.t && !a.bias) return launch_fwd64_bf16(a, s);
-  if (a.d == 128 && a.mask_kind != FA_MASK_BLOCK_SPARSE) return launch_fwd128s_bf16(a, s);
+  if (a.d == 128) return launch_fwd128s_bf16(a, s);
   return a.d == 64 ? launch_fwd_d<64, 1>(a, s) : launch_fwd_d<128, 2>(a, s);
 }
 
