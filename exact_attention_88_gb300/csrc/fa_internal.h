@@ -146,8 +146,8 @@ cudaError_t launch_fwd_fp32(const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_fp32(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_wait_probe(unsigned long long limit_ns, int* status, cudaStream_t s);
 
-// Block-sparse work order (query tiles, key tiles, query-tile pairs, each
-// most work first) of a T x T tile mask: tile_order_len(T) int32.
+// Block-sparse work order (query tiles, then key tiles, each most work first)
+// of a T x T tile mask: tile_order_len(T) int32.
 constexpr int kMaxTileOrder = 4096;  // = the largest block-mask side the kernels accept
 int tile_order_len(int T);           // 0 when T is out of range
 cudaError_t launch_tile_order(const uint8_t* block_mask, int T, int causal, int32_t* out,

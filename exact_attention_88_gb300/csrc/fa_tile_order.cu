@@ -1,7 +1,7 @@
 // Work order of a block-sparse mask: the tiles of each kind sorted by the
 // work each carries, most first, so that a grid that gives one CTA per tile
-// row (forward, dQ), per tile column (dK/dV) or per pair of tile rows (the
-// d = 128 forward) starts its longest CTAs first instead of ending with them.
+// row (forward, dQ) or per tile column (dK/dV) starts its longest CTAs first
+// instead of ending with them.
 // The order changes only which CTA takes which tile, never what a tile
 // computes ("FlashAttention: Fast and Memory-Efficient Exact Attention with
 // IO-Awareness", summary page, "Extension: block-sparse FlashAttention": the
@@ -98,10 +98,9 @@ __device__ void place_by_count(const int* c, int n, int V, int* hist, int32_t* o
 template <bool kVec>
 __global__ void __launch_bounds__(kOrderThreads)
     tile_order_kernel(const uint8_t* __restrict__ bm, int T, int causal, int32_t* __restrict__ out) {
-  extern __shared__ int cnt[];  // rows [0, T), columns [T, 2T), pairs [2T, 2T + P), bins
+  extern __shared__ int cnt[];  // rows [0, T), columns [T, 2T), bins
   pdl_wait();  // the kernel ahead on the stream is done (it may read `out`)
   pdl_launch_dependents();
-  const int P = (T + 1) / 2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   for (int e = threadIdx.x; e < 2 * T; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -165,23 +164,19 @@ __global__ void __launch_bounds__(kOrderThreads)
     }
   }
   __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x)
-    cnt[2 * T + p] = cnt[2 * p] + (2 * p + 1 < T ? cnt[2 * p + 1] : 0);
-  __syncthreads();
   // every count is in shared memory: the output may now be overwritten
-  int* hist = cnt + 2 * T + P;  // 2T + 2 ints
+  int* hist = cnt + 2 * T;  // 2T + 2 ints
   place_by_count(cnt, T, T, hist, out);
   place_by_count(cnt + T, T, T, hist, out + T);
-  place_by_count(cnt + 2 * T, P, 2 * T, hist, out + 2 * T);
 }
 
 }  // namespace
 
-int tile_order_len(int T) { return (T < 1 || T > kMaxTileOrder) ? 0 : 2 * T + (T + 1) / 2; }
+int tile_order_len(int T) { return (T < 1 || T > kMaxTileOrder) ? 0 : 2 * T; }
 
 cudaError_t launch_tile_order(const uint8_t* block_mask, int T, int causal, int32_t* out,
                               cudaStream_t s) {
-  // counts (2T + P ints) and the counting sort's bins (2T + 2 ints): <= 72 KB
+  // counts (2T ints) and the counting sort's bins (2T + 2 ints): <= 64 KB
   const int smem = (tile_order_len(T) + 2 * T + 2) * (int)sizeof(int);
   const bool vec = T % 16 == 0 && (reinterpret_cast<uintptr_t>(block_mask) & 15u) == 0;
   auto kernel = vec ? tile_order_kernel<true> : tile_order_kernel<false>;

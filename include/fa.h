@@ -89,7 +89,6 @@ typedef struct {
  * fa_block_mask_order_len(T) int32 to tile_order:
  *   [0, T)              query tiles, most visible key tiles first
  *   [T, 2T)             key tiles, most query tiles that see them first
- *   [2T, 2T + (T+1)/2)  pairs of query tiles (2p, 2p+1), most first
  * counting with the causal restriction when causal = 1; ties keep the lower
  * index first.  Passed as fa_mask.tile_order, the kernels take their tiles in
  * that order; every tile is still computed exactly once and the results are

@@ -118,9 +118,9 @@ def test_fwd_rejects_bad_masks(fa):
 
 
 def test_block_mask_order_rules(fa):
-    # 2T + ceil(T/2) entries for 1 <= T <= 4096 (the block-mask limit), else 0
+    # 2T entries for 1 <= T <= 4096 (the block-mask limit), else 0
     assert [fa.fa_block_mask_order_len(t) for t in (1, 2, 3, 128, 4096)] == [
-        3, 5, 8, 320, 10240]
+        2, 4, 6, 256, 8192]
     assert fa.fa_block_mask_order_len(0) == 0 and fa.fa_block_mask_order_len(4097) == 0
     call = lambda bm=FAKE, T=8, causal=0, out=FAKE: fa.lib.fa_block_mask_order(
         bm, T, causal, out, None)
